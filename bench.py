@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode-attention step on GB300.
+
+One step = the whole hot path over one batch: fused per-head RMSNorm + neox
+RoPE on q/k with the k/v append (pkvqk_norm_rope_append), split-KV paged
+decode attention (pkvqk_paged_decode / _partials) and, when the split count
+is above 1, the LSE combine (pkvqk_lse_combine) — all through the C ABI.
+
+Default workload: Qwen3-0.6B decode, 16 q / 8 kv heads, head_dim 128, bf16,
+block_size 16, batch 64 x context 8192, shuffled block ids (2.15 GB of K/V
+per step, larger than L2, so no flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle as reference arm
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica (replicas only: the step has no exchange between GPUs).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak) and seq-steps/s vs batch×ctx"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    # name: (builder, kwargs, description)
+    "decode_64x8192": ("decode_uniform", {"batch": 64, "ctx": 8192},
+                       "Qwen3-0.6B decode 16q/8kv D128 bf16 bs16, batch 64 x ctx 8192"),
+    "decode_32x8192": ("decode_uniform", {"batch": 32, "ctx": 8192},
+                       "Qwen3-0.6B decode 16q/8kv D128 bf16 bs16, batch 32 x ctx 8192"),
+    "decode_long_8x32768": ("decode_long", {},
+                            "Qwen3-1.7B long-context decode 16q/8kv D128 bs16, batch 8 x ctx 32768"),
+    "decode_gqa8_64": ("decode_gqa8", {},
+                       "Qwen3-30B-A3B-like decode 32q/4kv D128 bs16, batch 64, ctx log-U[256,16384]"),
+    "verify_32x5": ("verify_causal", {},
+                    "speculative verify 16q/8kv D128 bs16, batch 32, 5 query tokens, prior U[2048,8192]"),
+}
+for _b in (1, 8, 32, 64):
+    for _c in (512, 2048, 8192):
+        WORKLOADS.setdefault(f"decode_{_b}x{_c}", ("decode_uniform", {"batch": _b, "ctx": _c},
+                             f"Qwen3-0.6B decode 16q/8kv D128 bf16 bs16, batch {_b} x ctx {_c}"))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(p):
+    """Algorithmic HBM bytes of one step (what the step must move at least).
+
+    decode: every visible K and V row once (seq_len * Hkv * D * 2 B * 2),
+            q (B*q_len*Hq*D*2), the bf16 output (same), 4 B per block-table
+            entry read; split partials are overhead and not counted.
+    append: q read + written, k and v read, k and v rows written to the cache.
+    """
+    D, Hq, Hkv = p.D, p.Hq, p.Hkv
+    kv = int(p.seq_lens_host.sum()) * Hkv * D * 2 * 2
+    qo = 2 * p.T * Hq * D * 2
+    pages = int(sum(-(-int(n) // p.block_size) for n in p.seq_lens_host))
+    decode = kv + qo + 4 * pages
+    append = 2 * p.T * Hq * D * 2 + 2 * p.T * Hkv * D * 2 + 2 * p.T * Hkv * D * 2
+    return decode, append
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, path):
+        self.path = path
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.fh = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline_sample(seconds=10.0, max_seqs=64, ctx=8192, seed=2024):
+    """Time the fp64 oracle on sequences of the benchmark workload's shape.
+
+    Runs in this process with whatever threads numpy uses; called from a
+    child process pinned to one BLAS thread so the core count is known.
+    """
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_qk_gb300 import workloads
+
+    done_seqs, done_bytes, elapsed = 0, 0, 0.0
+    chunk = 4
+    while done_seqs < max_seqs and elapsed < seconds:
+        p = workloads.decode_uniform(chunk, ctx, device="cpu", seed=seed + done_seqs)
+        q = p.q.view(__import__("torch").int16).numpy().view(np.uint16).reshape(chunk, 1, p.Hq, p.D)
+        kb = p.k_cache.view(__import__("torch").int16).numpy().view(np.uint16)
+        vb = p.v_cache.view(__import__("torch").int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
+        elapsed += time.perf_counter() - t0
+        done_seqs += chunk
+        done_bytes += step_bytes(p)[0]
+    return {"seqs": done_seqs, "ctx": ctx, "bytes": done_bytes, "seconds": elapsed}
+
+
+def run_cpu_baseline_child(seconds, max_seqs, ctx):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+           "--cpu-seconds", str(seconds), "--cpu-max-seqs", str(max_seqs), "--cpu-ctx", str(ctx)]
+    r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.decode(errors="replace")[-300:]}
+    return json.loads(r.stdout.decode().strip().splitlines()[-1])
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle timed on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    name = args.workload
+    builder, kw, desc = WORKLOADS[name]
+    ctx = kw.get("ctx", 8192)
+    # each step: the oracle over one sampled sequence of the workload's shape
+    import numpy as np
+    import torch
+
+    import oracle
+    from paged_kv_cache_qk_gb300 import workloads
+
+    seqs_per_step = 1
+    p = workloads.decode_uniform(seqs_per_step, ctx, device="cpu", seed=4242)
+    q = p.q.view(torch.int16).numpy().view(np.uint16).reshape(seqs_per_step, 1, p.Hq, p.D)
+    kb = p.k_cache.view(torch.int16).numpy().view(np.uint16)
+    vb = p.v_cache.view(torch.int16).numpy().view(np.uint16)
+    for _ in range(args.warmup):
+        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    nbytes = step_bytes(p)[0]
+    gbs = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "sample": f"{seqs_per_step} sequence(s) x ctx {ctx} per step"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{seqs_per_step} sequence x ctx {ctx} (16q/8kv, D128) per step; "
+                                   "numpy default threads"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkvqk", choices=["pkvqk", "reference"])
+    ap.add_argument("--workload", default="decode_64x8192", choices=sorted(WORKLOADS))
+    ap.add_argument("--num-splits", type=int, default=-1, help="-1: host heuristic")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-max-seqs", type=int, default=64)
+    ap.add_argument("--cpu-ctx", type=int, default=8192)
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+
+    if args.cpu_baseline_child:
+        print(json.dumps(cpu_baseline_sample(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)))
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_qk_gb300 import binding as lib
+    from paged_kv_cache_qk_gb300 import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    builder, kw, desc = WORKLOADS[args.workload]
+    p = getattr(workloads, builder)(device=dev, **kw)
+    decode_bytes, append_bytes = step_bytes(p)
+    rows_per_kv = p.q_len * p.Hq // p.Hkv
+    S = args.num_splits if args.num_splits > 0 else lib.choose_num_splits(
+        p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
+    ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    rows = p.B * p.q_len * p.Hq
+    ws_f = ws.view(torch.float32)
+    ws_o = ws_f[: rows * S * 128] if S > 1 else None
+    ws_lse = ws_f[rows * S * 128: rows * S * 129] if S > 1 else None
+    out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev)
+    q = p.q.clone()
+    stream = torch.cuda.current_stream()
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    big_inputs = decode_bytes > 4 * l2_bytes
+    flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+
+    def decode_only():
+        if S > 1:
+            lib.paged_decode_partials(q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, ws,
+                                      q_len=p.q_len, num_splits=S,
+                                      max_seq_len_hint=p.max_seq_len, stream=stream)
+        else:
+            lib.paged_decode(q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                             q_len=p.q_len, num_splits=1, max_seq_len_hint=p.max_seq_len,
+                             stream=stream)
+
+    def step(ev_a=None, ev_b=None):
+        lib.norm_rope_append(q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q, p.gamma_k,
+                             p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        decode_only()
+        if ev_b is not None:
+            ev_b.record(stream)
+        if S > 1:
+            lib.lse_combine(ws_o, ws_lse, rows, S, out, stream=stream)
+
+    launches_per_step = 2 + (1 if S > 1 else 0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                          else f"/tmp/pkvqk_bench_clocks_r{rank}.csv")
+    time.sleep(0.3)
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    torch.cuda.synchronize()
+    if big_inputs:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            step(*evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t0.elapsed_time(t1)
+    else:
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            step_ev[i][0].record(stream)
+            step(*evs[i])
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end: host (pinned) inputs in, host output back, every step
+    host_in = {n: getattr(p, n).cpu().pin_memory() for n in
+               ("q", "k", "v", "positions", "slot_mapping", "block_tables", "seq_lens")}
+    dev_in = {n: torch.empty_like(getattr(p, n)) for n in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    K_e2e = max(3, min(K, 500))
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        lib.norm_rope_append(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["positions"],
+                             dev_in["slot_mapping"], p.gamma_q, p.gamma_k, p.theta, p.eps,
+                             p.k_cache, p.v_cache, stream=stream)
+        nb = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+        lib.paged_decode(dev_in["q"], p.k_cache, p.v_cache, dev_in["block_tables"],
+                         dev_in["seq_lens"], out, q_len=p.q_len, num_splits=S,
+                         max_seq_len_hint=p.max_seq_len, workspace=ws if nb else None,
+                         stream=stream)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K_e2e
+    clk = clocks.stop()
+
+    ms = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    bytes_step = decode_bytes + append_bytes
+    value = world * bytes_step / (ms * 1e-3) / 1e9
+    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    peak, peak_kind = load_peaks()
+    dec_avg_ms = statistics.fmean(decode_ms)
+    achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": desc,
+            "batch": p.B, "ctx_max": p.max_seq_len, "total_tokens": p.total_tokens,
+            "q_len": p.q_len, "heads_q": p.Hq, "heads_kv": p.Hkv, "head_dim": p.D,
+            "block_size": p.block_size, "num_splits": S,
+            "l2": ("inputs larger than L2: %.2f GB of K/V per step vs %d MB L2" %
+                   (decode_bytes / 1e9, l2_bytes >> 20)) if big_inputs else
+                  "L2 flushed (2x L2 write) before every step, excluded from timing",
+            "parallelism": f"replicas x{world}",
+        },
+        "seq_steps_per_s": round(world * p.B / (ms * 1e-3), 1),
+        "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": (K + args.warmup) * launches_per_step,
+        "roofline": {
+            "kernel": "paged_decode_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": decode_bytes,
+            "avg_launch_ms": round(dec_avg_ms, 5),
+        },
+        "clocks": clk,
+    }
+    line["gpu_launches_timed"] = K * launches_per_step
+    line["gpu_launches"] = K * launches_per_step + K_e2e * launches_per_step
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = run_cpu_baseline_child(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)
+        if "error" in cb:
+            line["cpu_baseline"] = {"error": cb["error"]}
+        else:
+            line["cpu_baseline"] = {
+                "value": round(cb["bytes"] / cb["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"{cb['seqs']} sequences x ctx {cb['ctx']} of the 16q/8kv D128 decode "
+                          f"workload, fp64 numpy oracle, 1 BLAS thread, {cb['seconds']:.1f} s",
+            }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,235 @@
+/*
+ * pkvqk — paged KV-cache decode attention for GB300 (sm_103a): C ABI.
+ *
+ * The decode step of an attention layer over a paged KV cache, in three
+ * calls that follow the problem statement of InfiniLM PR #585 ("perf: Qwen3
+ * offline inference — hybrid attention backend, fused rms_norm_rope, chunked
+ * prefill + prompt-lookup spec decoding"), section "概述 / Summary":
+ *
+ *   1. pkvqk_norm_rope_append — item 2: fused per-head RMSNorm + full-rotary
+ *      (neox rotate-half) RoPE on q and k; k and v then go into the paged
+ *      BSHD cache (item 1) through a slot mapping.
+ *   2. pkvqk_paged_decode     — item 1: split-KV paged decode attention with
+ *      GQA read straight from the strided BSHD cache; with q_len > 1 it is
+ *      the causal multi-query verify of item 4 (k + 1 tokens per sequence).
+ *   3. pkvqk_lse_combine      — item 1 ("splitkv"): log-sum-exp merge of the
+ *      split partials.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every buffer is owned by the caller; the library allocates no device
+ *   memory and keeps no state beyond a per-thread error message and a cached
+ *   per-device SM count.
+ * - Pointers marked "device" must be device (or managed) memory of the
+ *   current device; they are checked with cudaPointerGetAttributes and a
+ *   host pointer is rejected with PKVQK_ERR_POINTER_RESIDENCY.
+ * - bf16 means IEEE bfloat16 (raw 16-bit storage).  Strides are in elements.
+ * - Work is enqueued on `stream`; no call synchronises, reads device memory
+ *   on the host, or allocates, so every call can be recorded into a CUDA
+ *   graph.  Argument errors are detected on the host before any launch and
+ *   leave all buffers untouched.
+ * - `status_flags` (optional, may be NULL) is a device int32 into which the
+ *   kernels OR the PKVQK_FLAG_* bits below when they meet bad data (an
+ *   out-of-range block id or slot) or a pipeline wait that timed out.  The
+ *   caller zeroes it and reads it back when convenient.
+ * - On failure the call returns a non-zero pkvqk_status and
+ *   pkvqk_last_error() describes it.
+ */
+#ifndef PKVQK_H
+#define PKVQK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKVQK_API __attribute__((visibility("default")))
+#else
+#define PKVQK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* pkvqk_stream_t;
+
+typedef enum pkvqk_status {
+  PKVQK_OK = 0,
+  PKVQK_ERR_INVALID_ARG = 1,          /* null pointer, bad size, misaligned   */
+  PKVQK_ERR_UNSUPPORTED = 2,          /* valid but not implemented (e.g. D)   */
+  PKVQK_ERR_WORKSPACE_TOO_SMALL = 3,
+  PKVQK_ERR_POINTER_RESIDENCY = 4,    /* host pointer where device expected   */
+  PKVQK_ERR_CUDA = 5                  /* a CUDA runtime/driver call failed    */
+} pkvqk_status;
+
+/* Bits OR-ed into *status_flags by the kernels. */
+#define PKVQK_FLAG_BAD_SLOT      0x1  /* slot >= num_blocks*block_size: skipped */
+#define PKVQK_FLAG_BAD_BLOCK_ID  0x2  /* block id outside [0, num_blocks): its keys read as zeros */
+#define PKVQK_FLAG_WAIT_TIMEOUT  0x4  /* a pipeline wait gave up: output invalid */
+
+/*
+ * Layout of a paged cache, shared by the K and the V cache of a layer:
+ * element (block, slot, head, d) lives at
+ *     base + block*block_stride + slot*slot_stride + head*head_stride + d.
+ * The default BSHD layout [num_blocks, block_size, num_kv_heads, head_dim]
+ * has block_stride = block_size*num_kv_heads*head_dim,
+ * slot_stride = num_kv_heads*head_dim, head_stride = head_dim; any strides
+ * that are multiples of 8 elements (16 bytes) are accepted, so K and V may be
+ * two views into one interleaved or stacked allocation (no copy is made).
+ * block_size must be a multiple of 16 (16..256); head_dim must be 128.
+ */
+typedef struct pkvqk_cache_layout {
+  int64_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t reserved;                  /* set to 0 */
+  int64_t block_stride;
+  int64_t slot_stride;
+  int64_t head_stride;
+} pkvqk_cache_layout;
+
+/* Message of the last failing call made on this thread ("" if none). */
+PKVQK_API const char* pkvqk_last_error(void);
+
+/* ABI version of this header: 1. */
+PKVQK_API int32_t pkvqk_abi_version(void);
+
+/*
+ * Fused per-head RMSNorm + neox RoPE on q and k, then the k/v append.
+ * Source: InfiniLM PR #585, "概述 / Summary" item 2 ("rms_norm_rope"), item 1
+ * (BSHD paged cache).
+ *
+ * For each token t < num_tokens and head h, with x the head's D values:
+ *   y = x / sqrt(mean(x^2) + eps) * gamma          (gamma_q for q, gamma_k for k)
+ *   for i < D/2, a = positions[t] * theta^(-2i/D):
+ *     y'[i]       = y[i] cos a - y[i + D/2] sin a
+ *     y'[i + D/2] = y[i + D/2] cos a + y[i] sin a
+ * rounded once to bf16 (round-to-nearest-even).  q is overwritten in place.
+ * With s = slot_mapping[t] in [0, num_blocks*block_size), the rotated k and
+ * the unchanged v of every kv head go to block s / block_size, slot
+ * s % block_size of k_cache / v_cache.  s < 0 (padding) writes nothing; a
+ * too-large s writes nothing and sets PKVQK_FLAG_BAD_SLOT.
+ *
+ *   q             device bf16, element (t, h, d) at q[t*q_stride_t + h*q_stride_h + d]
+ *   k, v          device bf16, same form with their own strides, Hkv heads
+ *   positions     device int64 [num_tokens]
+ *   slot_mapping  device int64 [num_tokens]
+ *   gamma_q/_k    device bf16 [head_dim]
+ *   k_cache, v_cache  device bf16, layout as described by `layout`
+ * Two tokens mapped to the same slot race (caller error).  Strides and base
+ * pointers must be 16-byte aligned.
+ */
+PKVQK_API pkvqk_status pkvqk_norm_rope_append(
+    void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k, int64_t k_stride_t, int64_t k_stride_h,
+    const void* v, int64_t v_stride_t, int64_t v_stride_h,
+    const int64_t* positions, const int64_t* slot_mapping,
+    const void* gamma_q, const void* gamma_k,
+    float theta, float eps,
+    int32_t num_tokens, int32_t num_q_heads,
+    void* k_cache, void* v_cache, const pkvqk_cache_layout* layout,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/*
+ * Split count for pkvqk_paged_decode from host-side facts only (no device
+ * read): batch, kv heads, rows per kv head (q_len * Hq/Hkv), the longest
+ * sequence, the total key count and the SM count (0 = query the current
+ * device).  Returns a value in [1, 256].  Source: the "decode routing hint
+ * (host side, zero device sync)" of InfiniLM PR #585, Summary item 3.
+ */
+PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
+                                int32_t rows_per_kv_head, int32_t max_seq_len,
+                                int64_t total_tokens, int32_t block_size,
+                                int32_t sm_count);
+
+/*
+ * Workspace bytes pkvqk_paged_decode needs: 0 when num_splits == 1, else
+ * batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up to 256.
+ * Layout: fp32 partial outputs [rows][num_splits][head_dim] followed by
+ * fp32 partial lse [rows][num_splits], rows = (b*q_len + t)*Hq + h.
+ */
+PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
+                                    int32_t num_q_heads, int32_t head_dim,
+                                    int32_t num_splits);
+
+/*
+ * Split-KV paged decode attention with GQA; causal multi-query verify when
+ * q_len > 1.  Source: InfiniLM PR #585, "概述 / Summary" items 1 and 4.
+ *
+ * For sequence b, query token t < q_len and q head h (kv head h / (Hq/Hkv)):
+ *   visible keys  n < seq_lens[b] - q_len + t + 1, key n at block
+ *                 block_tables[b*max_blocks_per_seq + n / block_size],
+ *                 slot n % block_size
+ *   s_n = scale * <q, K_n>   (scale <= 0 selects head_dim^-1/2)
+ *   out = sum_n softmax(s)_n V_n,  lse = log sum_n exp(s_n)
+ * A row with no visible key outputs 0 and lse = -inf.
+ *
+ * Splits: with C = ceil(ceil(max_seq_len_hint / block_size) / num_splits)
+ * pages, split j < S-1 of a sequence covers pages [j*C, (j+1)*C) and split
+ * S-1 covers [(S-1)*C, end), so every key is covered whatever the hint.
+ * Each split keeps an online softmax; for num_splits > 1 the partials go to
+ * the workspace and pkvqk_lse_combine merges them (launched by this call).
+ *
+ *   q             device bf16, element (b*q_len + t, h, d) at
+ *                 q[(b*q_len + t)*q_stride_t + h*q_stride_h + d]
+ *   block_tables  device int32 [batch, max_blocks_per_seq]
+ *   seq_lens      device int32 [batch], counting the q_len new tokens
+ *   num_splits    1..256, or 0 = pkvqk_choose_num_splits(batch, Hkv,
+ *                 q_len*Hq/Hkv, hint, batch*hint, block_size, 0) with hint
+ *                 the effective max_seq_len_hint (size the workspace for it)
+ *   max_seq_len_hint  host int >= the longest seq_len (0 = max_blocks_per_seq*block_size)
+ *   out           device bf16 [batch, q_len, Hq, head_dim], contiguous
+ *   lse_out       device fp32 [batch, q_len, Hq] or NULL
+ *   workspace     device, >= pkvqk_decode_workspace_bytes(...) (NULL if 0)
+ * Supported: head_dim 128, Hq % Hkv == 0, q_len*Hq/Hkv <= 16.
+ */
+PKVQK_API pkvqk_status pkvqk_paged_decode(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k_cache, const void* v_cache, const pkvqk_cache_layout* layout,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens,
+    int32_t batch, int32_t q_len, int32_t num_q_heads,
+    int32_t num_splits, int32_t max_seq_len_hint, float scale,
+    void* out, float* lse_out,
+    void* workspace, size_t workspace_bytes,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/*
+ * As pkvqk_paged_decode but stops after the split pass: the partials stay in
+ * the workspace (layout above) and no combine is launched.  num_splits must
+ * be >= 2 (no heuristic).
+ */
+PKVQK_API pkvqk_status pkvqk_paged_decode_partials(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k_cache, const void* v_cache, const pkvqk_cache_layout* layout,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens,
+    int32_t batch, int32_t q_len, int32_t num_q_heads,
+    int32_t num_splits, int32_t max_seq_len_hint, float scale,
+    void* workspace, size_t workspace_bytes,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/*
+ * Log-sum-exp merge of split partials.  Source: InfiniLM PR #585, Summary
+ * item 1 ("splitkv").  For each row r < rows:
+ *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M)
+ *   out[r] = sum_j w_j o[r][j] / sum_j w_j,  lse_out[r] = M + log sum_j w_j
+ * Splits with lse = -inf weigh 0; a row whose splits are all empty outputs
+ * 0 and -inf.
+ *   ws_o    device fp32 [rows][num_splits][head_dim]
+ *   ws_lse  device fp32 [rows][num_splits]
+ *   out     device bf16 [rows][head_dim];  lse_out device fp32 [rows] or NULL
+ * head_dim must be 128.
+ */
+PKVQK_API pkvqk_status pkvqk_lse_combine(const float* ws_o, const float* ws_lse,
+                               int32_t rows, int32_t head_dim,
+                               int32_t num_splits, void* out, float* lse_out,
+                               pkvqk_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* PKVQK_H */

@@ -1,0 +1,446 @@
+// C-ABI host layer of pkvqk: argument validation, TMA descriptor encoding,
+// the split-count heuristic and kernel launches on the caller's stream.
+//
+// Nothing here allocates device memory, synchronises or reads device memory;
+// every decision comes from host arguments (InfiniLM PR #585, "概述 /
+// Summary" item 3: decode routing decided on the host with zero device sync),
+// so every entry point can be recorded into a CUDA graph.
+#include "../../include/pkvqk.h"
+#include "kernels.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pkvqk_status fail(pkvqk_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+pkvqk_status ok() {
+  g_last_error.clear();
+  return PKVQK_OK;
+}
+
+pkvqk_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKVQK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device pointer check (InfiniLM issue #498 review notes: host-resident vs
+// device-resident arguments are checked before use).
+pkvqk_status check_device_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(PKVQK_ERR_INVALID_ARG, "%s is NULL", name);
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(PKVQK_ERR_POINTER_RESIDENCY, "%s: cudaPointerGetAttributes failed (%s)", name,
+                cudaGetErrorName(e));
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(PKVQK_ERR_POINTER_RESIDENCY, "%s is not device memory", name);
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && attr.type == cudaMemoryTypeDevice && attr.device != dev)
+    return fail(PKVQK_ERR_POINTER_RESIDENCY, "%s lives on device %d, current device is %d", name,
+                attr.device, dev);
+  return PKVQK_OK;
+}
+
+#define PKVQK_TRY(expr)                      \
+  do {                                       \
+    pkvqk_status _s = (expr);                \
+    if (_s != PKVQK_OK) return _s;           \
+  } while (0)
+
+pkvqk_status check_layout(const pkvqk_cache_layout* L) {
+  if (L == nullptr) return fail(PKVQK_ERR_INVALID_ARG, "layout is NULL");
+  if (L->head_dim != 128) return fail(PKVQK_ERR_UNSUPPORTED, "head_dim %d (only 128)", L->head_dim);
+  if (L->num_blocks < 1 || L->num_blocks > (int64_t(1) << 31) - 1)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_blocks %lld out of range",
+                static_cast<long long>(L->num_blocks));
+  if (L->block_size < 16 || L->block_size > 256 || (L->block_size % 16) != 0)
+    return fail(PKVQK_ERR_UNSUPPORTED, "block_size %d (multiple of 16 in [16, 256])",
+                L->block_size);
+  if (L->num_kv_heads < 1 || L->num_kv_heads > 256)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_kv_heads %d", L->num_kv_heads);
+  const int64_t st[3] = {L->block_stride, L->slot_stride, L->head_stride};
+  const char* nm[3] = {"block_stride", "slot_stride", "head_stride"};
+  for (int i = 0; i < 3; ++i) {
+    if (st[i] <= 0 || (st[i] % 8) != 0 || st[i] * 2 >= (int64_t(1) << 40))
+      return fail(PKVQK_ERR_INVALID_ARG, "%s %lld must be a positive multiple of 8 elements", nm[i],
+                  static_cast<long long>(st[i]));
+  }
+  return PKVQK_OK;
+}
+
+// ------------------------------------------------------- TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+pkvqk_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr)
+    return fail(PKVQK_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                cudaGetErrorName(g_encode_err));
+  return PKVQK_OK;
+}
+
+// 5-D view of a paged cache for the decode kernel's TMA boxes:
+//   dims (inner first) = (64 dims, slot, dim half, kv head, block),
+// box = (64, 16 slots, 2, heads_per_cta, 1 block), 128-byte swizzle, so the
+// shared-memory tile of one (kv head, half) is 16 slot rows of 128 bytes.
+pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_cache_layout& L,
+                              int heads_per_cta) {
+  PKVQK_TRY(get_encoder());
+  cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(L.block_size), 2,
+                        static_cast<cuuint64_t>(L.num_kv_heads),
+                        static_cast<cuuint64_t>(L.num_blocks)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(L.slot_stride) * 2, 128,
+                           static_cast<cuuint64_t>(L.head_stride) * 2,
+                           static_cast<cuuint64_t>(L.block_stride) * 2};
+  cuuint32_t box[5] = {64, 16, 2, static_cast<cuuint32_t>(heads_per_cta), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKVQK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return PKVQK_OK;
+}
+
+// ---------------------------------------------------------------- SM count
+
+int sm_count_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Bytes of the fp32 partials [rows][S][128] + partial lse [rows][S].
+size_t partial_bytes(int64_t rows, int S) {
+  const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
+  return (raw + 255) & ~size_t(255);
+}
+
+struct DecodeCall {
+  const void* q;
+  int64_t q_stride_t, q_stride_h;
+  const void* k_cache;
+  const void* v_cache;
+  const pkvqk_cache_layout* layout;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int32_t batch, q_len, num_q_heads, num_splits, max_seq_len_hint;
+  float scale;
+  void* out;
+  float* lse_out;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status_flags;
+  cudaStream_t stream;
+  bool partials_only;
+};
+
+pkvqk_status run_decode(const DecodeCall& c) {
+  PKVQK_TRY(check_layout(c.layout));
+  const pkvqk_cache_layout& L = *c.layout;
+  if (c.batch < 0 || c.batch > 65535) return fail(PKVQK_ERR_INVALID_ARG, "batch %d", c.batch);
+  if (c.q_len < 1 || c.q_len > 16) return fail(PKVQK_ERR_INVALID_ARG, "q_len %d (1..16)", c.q_len);
+  if (c.num_q_heads < 1 || (c.num_q_heads % L.num_kv_heads) != 0)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                c.num_q_heads, L.num_kv_heads);
+  const int group = c.num_q_heads / L.num_kv_heads;
+  const int rows = c.q_len * group;
+  if (rows > 16)
+    return fail(PKVQK_ERR_UNSUPPORTED, "q_len * group = %d rows per kv head (max 16)", rows);
+  if (c.max_blocks_per_seq < 1) return fail(PKVQK_ERR_INVALID_ARG, "max_blocks_per_seq < 1");
+  if (c.max_seq_len_hint < 0) return fail(PKVQK_ERR_INVALID_ARG, "max_seq_len_hint < 0");
+  if (c.num_splits < 0 || c.num_splits > 256)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_splits %d (0..256)", c.num_splits);
+  if (c.partials_only && c.num_splits < 2)
+    return fail(PKVQK_ERR_INVALID_ARG, "partials need an explicit num_splits >= 2");
+  if (c.q_stride_t % 8 || c.q_stride_h % 8 || c.q_stride_h < 1 || c.q_stride_t < 0)
+    return fail(PKVQK_ERR_INVALID_ARG, "q strides must be multiples of 8 elements");
+  if (!std::isfinite(c.scale)) return fail(PKVQK_ERR_INVALID_ARG, "scale is not finite");
+
+  const int64_t cap_tokens = static_cast<int64_t>(c.max_blocks_per_seq) * L.block_size;
+  const int hint = c.max_seq_len_hint > 0
+                       ? c.max_seq_len_hint
+                       : static_cast<int>(std::min<int64_t>(cap_tokens, INT32_MAX));
+  int S = c.num_splits;
+  if (S == 0)
+    S = pkvqk_choose_num_splits(c.batch, L.num_kv_heads, rows, hint,
+                                static_cast<int64_t>(hint) * c.batch, L.block_size, 0);
+  const int64_t nrows = static_cast<int64_t>(c.batch) * c.q_len * c.num_q_heads;
+  const bool use_ws = c.partials_only || S > 1;
+  const size_t need_exact = use_ws ? partial_bytes(nrows, S) : 0;
+  if (use_ws && c.workspace_bytes < need_exact)
+    return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
+                c.workspace_bytes, need_exact);
+  if (c.batch == 0) return ok();
+
+  PKVQK_TRY(check_device_ptr(c.q, "q"));
+  PKVQK_TRY(check_device_ptr(c.k_cache, "k_cache"));
+  PKVQK_TRY(check_device_ptr(c.v_cache, "v_cache"));
+  PKVQK_TRY(check_device_ptr(c.block_tables, "block_tables"));
+  PKVQK_TRY(check_device_ptr(c.seq_lens, "seq_lens"));
+  if (!aligned16(c.q)) return fail(PKVQK_ERR_INVALID_ARG, "q not 16-byte aligned");
+  if (!aligned16(c.k_cache) || !aligned16(c.v_cache))
+    return fail(PKVQK_ERR_INVALID_ARG, "cache base not 16-byte aligned");
+  if (!c.partials_only) {
+    PKVQK_TRY(check_device_ptr(c.out, "out"));
+    if (!aligned16(c.out)) return fail(PKVQK_ERR_INVALID_ARG, "out not 16-byte aligned");
+    if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
+  }
+  if (use_ws) {
+    PKVQK_TRY(check_device_ptr(c.workspace, "workspace"));
+    if (!aligned16(c.workspace)) return fail(PKVQK_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  }
+  if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
+
+  const pkvqk::DecodePlan plan = pkvqk::plan_decode(L.num_kv_heads, rows);
+  CUtensorMap kmap, vmap;
+  PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta));
+  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta));
+
+  const int hint_pages = (hint + L.block_size - 1) / L.block_size;
+  pkvqk::DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(c.q);
+  a.q_stride_t = c.q_stride_t;
+  a.q_stride_h = c.q_stride_h;
+  a.block_tables = c.block_tables;
+  a.max_blocks_per_seq = c.max_blocks_per_seq;
+  a.seq_lens = c.seq_lens;
+  a.batch = c.batch;
+  a.q_len = c.q_len;
+  a.num_q_heads = c.num_q_heads;
+  a.num_kv_heads = L.num_kv_heads;
+  a.group = group;
+  a.block_size = L.block_size;
+  a.num_blocks = L.num_blocks;
+  a.num_splits = S;
+  a.chunk_pages = std::max(1, (hint_pages + S - 1) / S);
+  const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(128.0f);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = static_cast<__nv_bfloat16*>(c.out);
+  a.lse_out = c.lse_out;
+  a.ws_o = use_ws ? static_cast<float*>(c.workspace) : nullptr;
+  a.ws_lse = use_ws ? static_cast<float*>(c.workspace) + nrows * S * 128 : nullptr;
+  a.status_flags = c.status_flags;
+
+  cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  if (S > 1 && !c.partials_only) {
+    e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
+                                  c.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkvqk_last_error(void) { return g_last_error.c_str(); }
+
+int32_t pkvqk_abi_version(void) { return 1; }
+
+pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                    const void* k, int64_t k_stride_t, int64_t k_stride_h,
+                                    const void* v, int64_t v_stride_t, int64_t v_stride_h,
+                                    const int64_t* positions, const int64_t* slot_mapping,
+                                    const void* gamma_q, const void* gamma_k, float theta,
+                                    float eps, int32_t num_tokens, int32_t num_q_heads,
+                                    void* k_cache, void* v_cache,
+                                    const pkvqk_cache_layout* layout, int32_t* status_flags,
+                                    pkvqk_stream_t stream) {
+  PKVQK_TRY(check_layout(layout));
+  const pkvqk_cache_layout& L = *layout;
+  if (num_tokens < 0 || num_tokens > (1 << 30))
+    return fail(PKVQK_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+  if (num_q_heads < 1 || num_q_heads + L.num_kv_heads > 4096)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_q_heads %d", num_q_heads);
+  if (!(theta > 0.f) || !std::isfinite(theta)) return fail(PKVQK_ERR_INVALID_ARG, "theta must be > 0");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(PKVQK_ERR_INVALID_ARG, "eps must be >= 0");
+  const int64_t st[6] = {q_stride_t, q_stride_h, k_stride_t, k_stride_h, v_stride_t, v_stride_h};
+  for (int i = 0; i < 6; ++i)
+    if (st[i] < 0 || (st[i] % 8) != 0)
+      return fail(PKVQK_ERR_INVALID_ARG, "q/k/v strides must be non-negative multiples of 8");
+  if (num_tokens == 0) return ok();
+  PKVQK_TRY(check_device_ptr(q, "q"));
+  PKVQK_TRY(check_device_ptr(k, "k"));
+  PKVQK_TRY(check_device_ptr(v, "v"));
+  PKVQK_TRY(check_device_ptr(positions, "positions"));
+  PKVQK_TRY(check_device_ptr(slot_mapping, "slot_mapping"));
+  PKVQK_TRY(check_device_ptr(gamma_q, "gamma_q"));
+  PKVQK_TRY(check_device_ptr(gamma_k, "gamma_k"));
+  PKVQK_TRY(check_device_ptr(k_cache, "k_cache"));
+  PKVQK_TRY(check_device_ptr(v_cache, "v_cache"));
+  if (status_flags != nullptr) PKVQK_TRY(check_device_ptr(status_flags, "status_flags"));
+  const void* al[7] = {q, k, v, gamma_q, gamma_k, k_cache, v_cache};
+  for (int i = 0; i < 7; ++i)
+    if (!aligned16(al[i])) return fail(PKVQK_ERR_INVALID_ARG, "bf16 base pointer not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(positions) & 7u) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return fail(PKVQK_ERR_INVALID_ARG, "positions/slot_mapping not 8-byte aligned");
+
+  pkvqk::NormRopeAppendArgs a;
+  a.q = static_cast<__nv_bfloat16*>(q);
+  a.q_stride_t = q_stride_t;
+  a.q_stride_h = q_stride_h;
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.k_stride_t = k_stride_t;
+  a.k_stride_h = k_stride_h;
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.v_stride_t = v_stride_t;
+  a.v_stride_h = v_stride_h;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
+  a.gamma_k = static_cast<const __nv_bfloat16*>(gamma_k);
+  a.theta = theta;
+  a.eps = eps;
+  a.num_tokens = num_tokens;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = L.num_kv_heads;
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.num_blocks = L.num_blocks;
+  a.block_size = L.block_size;
+  a.block_stride = L.block_stride;
+  a.slot_stride = L.slot_stride;
+  a.head_stride = L.head_stride;
+  a.status_flags = status_flags;
+  cudaError_t e = pkvqk::launch_norm_rope_append(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "norm_rope_append launch");
+  return ok();
+}
+
+int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t rows_per_kv_head,
+                                int32_t max_seq_len, int64_t total_tokens, int32_t block_size,
+                                int32_t sm_count) {
+  (void)rows_per_kv_head;
+  if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0 || block_size <= 0) return 1;
+  if (sm_count <= 0) sm_count = sm_count_current();
+  const pkvqk::DecodePlan plan = pkvqk::plan_decode(num_kv_heads, rows_per_kv_head);
+  const int64_t groups = num_kv_heads / plan.heads_per_cta;
+  const int64_t max_pages = (max_seq_len + block_size - 1) / block_size;
+  const int64_t tot_pages =
+      std::max<int64_t>((total_tokens + block_size - 1) / block_size, max_pages);
+  // Model: one resident CTA per SM; a wave of CTAs lasts as long as its
+  // longest split (chunk pages) plus a fixed start-up cost worth ~2 pages.
+  const double startup_pages = 2.0;
+  double best_t = 1e300;
+  int best = 1;
+  for (int S = 1; S <= 256; ++S) {
+    const int64_t chunk = (max_pages + S - 1) / S;
+    if (S > 1 && chunk * S - chunk >= max_pages) continue;          // an always-empty split
+    const int64_t splits_per_seq_avg =
+        std::max<int64_t>(1, (tot_pages + batch * chunk - 1) / (batch * chunk));
+    const int64_t ctas = groups * batch * std::min<int64_t>(splits_per_seq_avg, S);
+    const int64_t waves = (ctas + sm_count - 1) / sm_count;
+    double t = static_cast<double>(waves) * (static_cast<double>(chunk) + startup_pages);
+    if (S > 1) t += 0.5;                                             // combine launch
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best;
+}
+
+size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                    int32_t head_dim, int32_t num_splits) {
+  if (batch <= 0 || q_len <= 0 || num_q_heads <= 0 || head_dim != 128 || num_splits <= 1) return 0;
+  return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits);
+}
+
+pkvqk_status pkvqk_paged_decode(const void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                const void* k_cache, const void* v_cache,
+                                const pkvqk_cache_layout* layout, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                int32_t num_splits, int32_t max_seq_len_hint, float scale,
+                                void* out, float* lse_out, void* workspace,
+                                size_t workspace_bytes_, int32_t* status_flags,
+                                pkvqk_stream_t stream) {
+  DecodeCall c{q,          q_stride_t,  q_stride_h,       k_cache,    v_cache,
+               layout,     block_tables, max_blocks_per_seq, seq_lens, batch,
+               q_len,      num_q_heads, num_splits,       max_seq_len_hint, scale,
+               out,        lse_out,     workspace,        workspace_bytes_, status_flags,
+               reinterpret_cast<cudaStream_t>(stream), false};
+  return run_decode(c);
+}
+
+pkvqk_status pkvqk_paged_decode_partials(const void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                         const void* k_cache, const void* v_cache,
+                                         const pkvqk_cache_layout* layout,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                                         int32_t num_q_heads, int32_t num_splits,
+                                         int32_t max_seq_len_hint, float scale, void* workspace,
+                                         size_t workspace_bytes_, int32_t* status_flags,
+                                         pkvqk_stream_t stream) {
+  DecodeCall c{q,          q_stride_t,  q_stride_h,       k_cache,    v_cache,
+               layout,     block_tables, max_blocks_per_seq, seq_lens, batch,
+               q_len,      num_q_heads, num_splits,       max_seq_len_hint, scale,
+               nullptr,    nullptr,     workspace,        workspace_bytes_, status_flags,
+               reinterpret_cast<cudaStream_t>(stream), true};
+  return run_decode(c);
+}
+
+pkvqk_status pkvqk_lse_combine(const float* ws_o, const float* ws_lse, int32_t rows,
+                               int32_t head_dim, int32_t num_splits, void* out, float* lse_out,
+                               pkvqk_stream_t stream) {
+  if (head_dim != 128) return fail(PKVQK_ERR_UNSUPPORTED, "head_dim %d (only 128)", head_dim);
+  if (rows < 0) return fail(PKVQK_ERR_INVALID_ARG, "rows %d", rows);
+  if (num_splits < 1 || num_splits > 256)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_splits %d (1..256)", num_splits);
+  if (rows == 0) return ok();
+  PKVQK_TRY(check_device_ptr(ws_o, "ws_o"));
+  PKVQK_TRY(check_device_ptr(ws_lse, "ws_lse"));
+  PKVQK_TRY(check_device_ptr(out, "out"));
+  if (lse_out != nullptr) PKVQK_TRY(check_device_ptr(lse_out, "lse_out"));
+  if (!aligned16(ws_o) || !aligned16(out))
+    return fail(PKVQK_ERR_INVALID_ARG, "ws_o/out not 16-byte aligned");
+  cudaError_t e = pkvqk::launch_lse_combine(ws_o, ws_lse, rows, num_splits,
+                                            static_cast<__nv_bfloat16*>(out), lse_out,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Internal launch interface between the C-ABI host layer (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkvqk {
+
+struct NormRopeAppendArgs {
+  __nv_bfloat16* q;
+  int64_t q_stride_t, q_stride_h;
+  const __nv_bfloat16* k;
+  int64_t k_stride_t, k_stride_h;
+  const __nv_bfloat16* v;
+  int64_t v_stride_t, v_stride_h;
+  const int64_t* positions;
+  const int64_t* slot_mapping;
+  const __nv_bfloat16* gamma_q;
+  const __nv_bfloat16* gamma_k;
+  float theta, eps;
+  int32_t num_tokens, num_q_heads, num_kv_heads;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  int64_t num_blocks;
+  int32_t block_size;
+  int64_t block_stride, slot_stride, head_stride;
+  int32_t* status_flags;
+};
+
+cudaError_t launch_norm_rope_append(const NormRopeAppendArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  int64_t q_stride_t, q_stride_h;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int32_t batch, q_len, num_q_heads, num_kv_heads, group;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t num_splits, chunk_pages;
+  float scale_log2;              // softmax scale * log2(e)
+  __nv_bfloat16* out;            // num_splits == 1: final bf16 output
+  float* lse_out;                // num_splits == 1: optional lse
+  float* ws_o;                   // num_splits > 1: partial outputs
+  float* ws_lse;                 // num_splits > 1: partial lse
+  int32_t* status_flags;
+};
+
+// Kernel family chosen by the host for a decode call.
+struct DecodePlan {
+  int heads_per_cta;   // kv heads handled by one CTA (divides num_kv_heads)
+  bool tensor_core;    // mma tiles (rows per kv head > 4) vs CUDA-core dots
+  int rows;            // q_len * group
+};
+
+DecodePlan plan_decode(int num_kv_heads, int rows);
+
+cudaError_t launch_paged_decode(const DecodePlan& plan, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, const DecodeArgs& a,
+                                cudaStream_t stream);
+
+cudaError_t launch_lse_combine(const float* ws_o, const float* ws_lse, int rows, int num_splits,
+                               __nv_bfloat16* out, float* lse_out, cudaStream_t stream);
+
+}  // namespace pkvqk

@@ -1,0 +1,133 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+* libpkvqk.so loads and exports every function include/pkvqk.h declares;
+* argument validation returns the documented status before any launch;
+* the host-only helpers (split heuristic, workspace size) follow their
+  documented formulas.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkvqk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_qk_gb300 import build
+    build.build()
+    from paged_kv_cache_qk_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"PKVQK_API\s+[\w\s\*]+?\b(pkvqk_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["pkvqk_norm_rope_append", "pkvqk_paged_decode", "pkvqk_lse_combine",
+              "pkvqk_choose_num_splits", "pkvqk_decode_workspace_bytes"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(so, n), f"{n} not exported"
+    assert set(declared_functions()) <= set(lib.EXPORTED)
+    assert lib.pkvqk_abi_version() == 1
+
+
+def _layout(lib, nb=64, bs=16, hkv=8, d=128, strides=None):
+    if strides is None:
+        strides = (bs * hkv * d, hkv * d, d)
+    return lib.CacheLayout(nb, bs, hkv, d, 0, *strides)
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails before pointer checks
+
+
+def _decode(lib, lay, B=4, q_len=1, Hq=16, S=1, hint=256, ws=0, maxp=16, qs=(2048, 128)):
+    return lib.pkvqk_paged_decode(FAKE, qs[0], qs[1], FAKE, FAKE, ctypes.byref(lay), FAKE, maxp,
+                                  FAKE, B, q_len, Hq, S, hint, 0.0, FAKE, None, FAKE, ws, None,
+                                  None)
+
+
+def test_decode_validation_errors(lib):
+    lay = _layout(lib)
+    assert _decode(lib, _layout(lib, d=64)) == lib.PKVQK_ERR_UNSUPPORTED
+    assert "head_dim" in lib.pkvqk_last_error().decode()
+    assert _decode(lib, _layout(lib, bs=8)) == lib.PKVQK_ERR_UNSUPPORTED
+    assert _decode(lib, _layout(lib, bs=24)) == lib.PKVQK_ERR_UNSUPPORTED
+    assert _decode(lib, lay, q_len=0) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, q_len=17) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, Hq=12) == lib.PKVQK_ERR_INVALID_ARG            # 12 % 8 != 0
+    assert _decode(lib, lay, Hq=64, q_len=3) == lib.PKVQK_ERR_UNSUPPORTED   # 24 rows per kv head
+    assert _decode(lib, lay, S=257) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, S=-1) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, S=4, ws=100) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
+    assert _decode(lib, lay, maxp=0) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, qs=(2048, 100)) == lib.PKVQK_ERR_INVALID_ARG   # q head stride % 8
+    assert _decode(lib, _layout(lib, strides=(16384, 1020, 128))) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, _layout(lib, nb=0)) == lib.PKVQK_ERR_INVALID_ARG
+    # batch 0 is a valid no-op
+    assert _decode(lib, lay, B=0) == lib.PKVQK_OK
+    assert lib.pkvqk_last_error().decode() == ""
+
+
+def test_partials_need_explicit_splits(lib):
+    lay = _layout(lib)
+    r = lib.pkvqk_paged_decode_partials(FAKE, 2048, 128, FAKE, FAKE, ctypes.byref(lay), FAKE, 16,
+                                        FAKE, 4, 1, 16, 1, 256, 0.0, FAKE, 1 << 20, None, None)
+    assert r == lib.PKVQK_ERR_INVALID_ARG
+
+
+def test_append_validation_errors(lib):
+    lay = _layout(lib)
+
+    def call(theta=1e6, eps=1e-6, T=4, Hq=16, lay=lay, qst=2048):
+        return lib.pkvqk_norm_rope_append(FAKE, qst, 128, FAKE, 1024, 128, FAKE, 1024, 128,
+                                          FAKE, FAKE, FAKE, FAKE, theta, eps, T, Hq, FAKE, FAKE,
+                                          ctypes.byref(lay), None, None)
+    assert call(theta=0.0) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(theta=float("nan")) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(eps=-1.0) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(T=-1) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(Hq=0) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(qst=2047) == lib.PKVQK_ERR_INVALID_ARG
+    assert call(lay=_layout(lib, d=256)) == lib.PKVQK_ERR_UNSUPPORTED
+    assert call(T=0) == lib.PKVQK_OK
+
+
+def test_combine_validation_errors(lib):
+    c = lib.pkvqk_lse_combine
+    assert c(FAKE, FAKE, 4, 64, 2, FAKE, None, None) == lib.PKVQK_ERR_UNSUPPORTED
+    assert c(FAKE, FAKE, -1, 128, 2, FAKE, None, None) == lib.PKVQK_ERR_INVALID_ARG
+    assert c(FAKE, FAKE, 4, 128, 0, FAKE, None, None) == lib.PKVQK_ERR_INVALID_ARG
+    assert c(FAKE, FAKE, 0, 128, 2, FAKE, None, None) == lib.PKVQK_OK
+
+
+def test_workspace_bytes_formula(lib):
+    assert lib.decode_workspace_bytes(4, 1, 16, 128, 1) == 0
+    for B, T, Hq, S in [(4, 1, 16, 4), (64, 1, 16, 19), (32, 5, 16, 8), (1, 1, 8, 2)]:
+        raw = B * T * Hq * S * 129 * 4
+        assert lib.decode_workspace_bytes(B, T, Hq, 128, S) == (raw + 255) // 256 * 256
+    assert lib.decode_workspace_bytes(4, 1, 16, 64, 4) == 0
+
+
+def test_split_heuristic_is_host_only_and_bounded(lib):
+    for B, hkv, rows, L, sms in [(1, 8, 2, 512, 148), (64, 8, 2, 8192, 152), (8, 8, 2, 32768, 152),
+                                 (64, 4, 8, 16384, 152), (32, 8, 10, 8197, 152), (4, 8, 2, 1, 152)]:
+        S = lib.choose_num_splits(B, hkv, rows, L, B * L, 16, sms)
+        assert 1 <= S <= 256
+        assert S <= max(1, -(-L // 16))           # never more splits than pages
+    # a single long sequence is spread over many splits; a full batch is not split much
+    assert lib.choose_num_splits(8, 8, 2, 32768, 8 * 32768, 16, 152) >= 8
+    assert lib.choose_num_splits(1, 8, 2, 512, 512, 16, 152) >= 2
+    assert lib.choose_num_splits(0, 8, 2, 512, 0, 16, 152) == 1
