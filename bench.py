@@ -286,14 +286,16 @@ def main():
                              q_len=p.q_len, num_splits=1, max_seq_len_hint=p.max_seq_len,
                              stream=stream)
 
-    def step(ev_a=None, ev_b=None):
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         lib.norm_rope_append(q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q, p.gamma_k,
                              p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
-        if ev_a is not None:
-            ev_a.record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         decode_only()
-        if ev_b is not None:
-            ev_b.record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         if S > 1:
             lib.lse_combine(ws_o, ws_lse, rows, S, out, stream=stream)
 
@@ -311,15 +313,14 @@ def main():
     time.sleep(0.3)
 
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     torch.cuda.synchronize()
     if big_inputs:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(K):
-            step(*evs[i])
+            step(evs[i])
         t1.record(stream)
         torch.cuda.synchronize()
         total_ms = t0.elapsed_time(t1)
@@ -329,11 +330,12 @@ def main():
         for i in range(K):
             flush.zero_()
             step_ev[i][0].record(stream)
-            step(*evs[i])
+            step(evs[i])
             step_ev[i][1].record(stream)
         torch.cuda.synchronize()
         total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
-    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    decode_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
     # end to end: host (pinned) inputs in, host output back, every step
     host_in = {n: getattr(p, n).cpu().pin_memory() for n in
@@ -410,7 +412,7 @@ def main():
         "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": (K + args.warmup) * launches_per_step,
+        "gpu_launches": K * launches_per_step,
         "roofline": {
             "kernel": "paged_decode_kernel",
             "bound": "hbm",
@@ -424,9 +426,9 @@ def main():
             "avg_launch_ms": round(dec_avg_ms, 5),
         },
         "clocks": clk,
+        "append_avg_ms": round(statistics.fmean(append_ms), 5),
+        "e2e_gpu_launches": K_e2e * launches_per_step,
     }
-    line["gpu_launches_timed"] = K * launches_per_step
-    line["gpu_launches"] = K * launches_per_step + K_e2e * launches_per_step
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = run_cpu_baseline_child(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)
         if "error" in cb:

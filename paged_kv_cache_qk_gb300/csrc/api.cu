@@ -331,8 +331,9 @@ pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_strid
   a.slot_mapping = slot_mapping;
   a.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
   a.gamma_k = static_cast<const __nv_bfloat16*>(gamma_k);
-  a.theta = theta;
   a.eps = eps;
+  for (int i = 0; i < 64; ++i)
+    a.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
   a.num_tokens = num_tokens;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = L.num_kv_heads;

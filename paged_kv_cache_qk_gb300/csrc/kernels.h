@@ -20,7 +20,8 @@ struct NormRopeAppendArgs {
   const int64_t* slot_mapping;
   const __nv_bfloat16* gamma_q;
   const __nv_bfloat16* gamma_k;
-  float theta, eps;
+  float eps;
+  double inv_freq[64];             // theta^(-2i/D), i < D/2, computed on the host in float64
   int32_t num_tokens, num_q_heads, num_kv_heads;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;

@@ -5,14 +5,21 @@
 // item 2 (per-head RMSNorm + full-rotary RoPE in one op) and item 1 (the
 // BSHD paged cache the decode kernel reads).
 //
-// One CTA per token.  The token's 64 rotation angles are computed once, in
-// float64 with an explicit 2*pi reduction (positions reach 3e4 rad, where a
-// float32 angle would be off by ~2e-3 rad), then sin/cos of the reduced
-// float32 angle go to shared memory for every head of the token.  Each head
-// vector (D = 128 bf16 = 256 B) is handled by a half-warp: lane l holds
-// elements [8l, 8l+8) as one 16-byte load; the sum of squares is a 4-step
-// xor-shuffle reduction inside the half-warp, and the rotate-half partner of
-// lane l is lane l ^ 8.
+// One CTA per token.  Numerics, chosen so the rounded bf16 result is within
+// one ulp of the correctly rounded exact value even where the rotation
+// cancels (y_i cos - y_{i+D/2} sin close to 0):
+//  * the token's 64 angles pos * inv_freq_i (inv_freq from the host, float64)
+//    are reduced by 2*pi and their sin/cos evaluated in float64 once per
+//    token, then kept in shared memory as float-float pairs (hi + lo);
+//  * per element a = x * gamma is exact in fp32 (two 8-bit significands);
+//    the rotation a_i c - a_j s is formed with error-free products
+//    (p = a*c_hi, e = fma(a, c_hi, -p)) so cancellation loses nothing;
+//  * the RMS scale r = rsqrt(mean(x^2) + eps) multiplies the rotated value
+//    last (a common factor, it contributes only relative error).
+// Each head vector (D = 128 bf16 = 256 B) is handled by a half-warp: lane l
+// holds elements [8l, 8l+8) as one 16-byte load; the sum of squares is a
+// 4-step xor-shuffle reduction inside the half-warp, and the rotate-half
+// partner of lane l is lane l ^ 8.
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -21,12 +28,14 @@ namespace pkvqk {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kTwoPiHi = 6.283185307179586232;          // 2*pi rounded to double
+constexpr double kTwoPiLo = 2.4492935982947064e-16;          // 2*pi - kTwoPiHi
+constexpr double kInvTwoPi = 0.15915494309189535;
 
 __global__ void __launch_bounds__(kThreads)
 norm_rope_append_kernel(NormRopeAppendArgs a) {
-  __shared__ float s_cos[kHeadDim / 2];
-  __shared__ float s_sin[kHeadDim / 2];
+  __shared__ float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
+  __shared__ float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
 
   const int t = blockIdx.x;
   const int64_t pos = a.positions[t];
@@ -35,14 +44,17 @@ norm_rope_append_kernel(NormRopeAppendArgs a) {
 
   if (threadIdx.x < kHeadDim / 2) {
     const int i = threadIdx.x;
-    const double inv_freq = pow(static_cast<double>(a.theta), -2.0 * i / kHeadDim);
-    const double ang = static_cast<double>(pos) * inv_freq;
-    const double turns = rint(ang * (1.0 / kTwoPi));
-    const double red = fma(-turns, kTwoPi, ang);        // in [-pi, pi]
-    float sn, cs;
-    sincosf(static_cast<float>(red), &sn, &cs);
-    s_cos[i] = cs;
-    s_sin[i] = sn;
+    const double ang = static_cast<double>(pos) * a.inv_freq[i];
+    const double turns = rint(ang * kInvTwoPi);
+    double red = fma(-turns, kTwoPiHi, ang);             // Cody-Waite: 2*pi = hi + lo
+    red = fma(-turns, kTwoPiLo, red);                     // |red| <= pi (+ rounding)
+    double sn, cs;
+    sincos(red, &sn, &cs);
+    const float ch = static_cast<float>(cs), sh = static_cast<float>(sn);
+    s_cos_hi[i] = ch;
+    s_cos_lo[i] = static_cast<float>(cs - static_cast<double>(ch));
+    s_sin_hi[i] = sh;
+    s_sin_lo[i] = static_cast<float>(sn - static_cast<double>(sh));
   }
   if (threadIdx.x == 0 && slot >= nslots) report(a.status_flags, kFlagBadSlot);
   __syncthreads();
@@ -86,25 +98,31 @@ norm_rope_append_kernel(NormRopeAppendArgs a) {
     unpack8(xv, x);
     unpack8(gv, g);
 
-    float ss = 0.f;
+    // x*gamma is exact in fp32; x^2 is exact, the sum rounds
+    float ss = 0.f, ag[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+    for (int j = 0; j < 8; ++j) {
+      ss = fmaf(x[j], x[j], ss);
+      ag[j] = x[j] * g[j];
+    }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(fmaf(ss, inv_d, a.eps));
 
-    float y[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = x[j] * r * g[j];
-
-    // rotate-half: lanes 0..7 hold y[i], lanes 8..15 hold y[i + D/2]
+    // rotate-half: lanes 0..7 hold a[i], lanes 8..15 hold a[i + D/2];
+    // out_i = a_i c - a_{i+D/2} s,  out_{i+D/2} = a_{i+D/2} c + a_i s
     const int fbase = (l & 7) * 8;
+    const float sgn = (l < 8) ? -1.f : 1.f;
     float out[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float partner = __shfl_xor_sync(0xffffffffu, y[j], 8);
-      const float c = s_cos[fbase + j], s = s_sin[fbase + j];
-      out[j] = (l < 8) ? fmaf(y[j], c, -partner * s) : fmaf(y[j], c, partner * s);
+      const float b = sgn * __shfl_xor_sync(0xffffffffu, ag[j], 8);
+      const float ch = s_cos_hi[fbase + j], cl = s_cos_lo[fbase + j];
+      const float sh = s_sin_hi[fbase + j], sl = s_sin_lo[fbase + j];
+      const float p1 = ag[j] * ch, e1 = fmaf(ag[j], ch, -p1);   // a*c_hi = p1 + e1 exactly
+      const float p2 = b * sh, e2 = fmaf(b, sh, -p2);           // b*s_hi = p2 + e2 exactly
+      const float tail = fmaf(ag[j], cl, b * sl) + (e1 + e2);
+      out[j] = r * ((p1 + p2) + tail);
     }
     uint4 ov;
     ov.x = pack_bf16x2(out[0], out[1]);

@@ -100,6 +100,23 @@ def test_block_size_256(lib):
     _run_and_check(lib, p)
 
 
+def test_cancellation_many_tokens_long_positions(lib):
+    """4096 tokens x 24 heads at positions up to 65535: the rotation
+    a_i cos - a_{i+D/2} sin lands near zero for some elements, where a plain
+    fp32 rotation is many ulps off; the bar stays 1 ulp."""
+    T, Hq, Hkv, D, bs, NB = 4096, 16, 8, 128, 16, 8
+    g = torch.Generator(device="cuda").manual_seed(912)
+    p = workloads.make_problem("cancel", Hq, Hkv, D, bs, [1], 1, NB, 912, "cuda")
+    p.q = torch.randn(T, Hq, D, generator=g, device="cuda").to(torch.bfloat16)
+    p.k = torch.randn(T, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    p.v = torch.randn(T, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    p.positions = torch.randint(0, 65536, (T,), generator=g, device="cuda")
+    slots = torch.full((T,), -1, dtype=torch.int64, device="cuda")
+    slots[:NB * bs] = torch.randperm(NB * bs, generator=g, device="cuda")
+    _, dq, dk = _run_and_check(lib, p, slots=slots)
+    assert dq.max() <= 1
+
+
 def test_zero_tokens_is_noop(lib):
     p = workloads.decode_tiny(device="cuda")
     kc = p.k_cache.clone()
