@@ -212,6 +212,39 @@ PKVQK_API pkvqk_status pkvqk_paged_decode_partials(
     int32_t* status_flags, pkvqk_stream_t stream);
 
 /*
+ * pkvqk_paged_decode without a caller workspace.  The pages describe no such
+ * call: it has no counterpart there and exists for callers that cannot
+ * allocate device memory — e.g. a plugin that a host engine hands only input
+ * and output pointers, or code running while an allocator refuses to
+ * allocate — and so cannot pass the split workspace.
+ *
+ * Same arguments and results as pkvqk_paged_decode minus workspace and
+ * workspace_bytes.  The split partials go to a fixed 16 MiB array inside the
+ * library (pkvqk_static_workspace_capacity()), held on every GPU that loads
+ * the library until the process exits.  A call whose partials need more
+ * (pkvqk_decode_workspace_bytes for its split count) returns
+ * PKVQK_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The call allocates
+ * nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the last call's partials: calls that can overlap on the GPU
+ * (different streams, no ordering between them) race and corrupt each
+ * other's results.  Nothing in it needs to start at zero.
+ */
+PKVQK_API pkvqk_status pkvqk_paged_decode_static_ws(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k_cache, const void* v_cache, const pkvqk_cache_layout* layout,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens,
+    int32_t batch, int32_t q_len, int32_t num_q_heads,
+    int32_t num_splits, int32_t max_seq_len_hint, float scale,
+    void* out, float* lse_out,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/* Bytes of the array pkvqk_paged_decode_static_ws uses (16 MiB). */
+PKVQK_API size_t pkvqk_static_workspace_capacity(void);
+
+/*
  * Log-sum-exp merge of split partials.  Source: InfiniLM PR #585, Summary
  * item 1 ("splitkv").  For each row r < rows:
  *   M = max_j lse[r][j];  w_j = exp(lse[r][j] - M)

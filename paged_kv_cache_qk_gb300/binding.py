@@ -90,11 +90,15 @@ pkvqk_paged_decode_partials = _sig("pkvqk_paged_decode_partials", ctypes.c_int,
                                    _decode_args + [c_vp, c_size, c_vp, c_vp])
 pkvqk_lse_combine = _sig("pkvqk_lse_combine", ctypes.c_int,
                          [c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp])
+pkvqk_paged_decode_static_ws = _sig("pkvqk_paged_decode_static_ws", ctypes.c_int,
+                                    _decode_args + [c_vp, c_vp, c_vp, c_vp])
+pkvqk_static_workspace_capacity = _sig("pkvqk_static_workspace_capacity", c_size, [])
 
 EXPORTED = [
     "pkvqk_last_error", "pkvqk_abi_version", "pkvqk_norm_rope_append",
     "pkvqk_choose_num_splits", "pkvqk_decode_workspace_bytes", "pkvqk_paged_decode",
-    "pkvqk_paged_decode_partials", "pkvqk_lse_combine",
+    "pkvqk_paged_decode_partials", "pkvqk_lse_combine", "pkvqk_paged_decode_static_ws",
+    "pkvqk_static_workspace_capacity",
 ]
 
 

@@ -273,6 +273,10 @@ pkvqk_status run_decode(const DecodeCall& c) {
 
 }  // namespace
 
+namespace pkvqk {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace pkvqk
+
 extern "C" {
 
 const char* pkvqk_last_error(void) { return g_last_error.c_str(); }
