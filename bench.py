@@ -49,6 +49,8 @@ WORKLOADS = {
     "verify_32x5": ("verify_causal", {},
                     "speculative verify 16q/8kv D128 bs16, batch 32, 5 query tokens, prior U[2048,8192]"),
 }
+WORKLOADS["decode_gqa8_64x4096"] = ("make_problem_uniform_gqa8", {},
+                                    "GQA-8 decode 32q/4kv D128 bs16, batch 64 x ctx 4096 (uniform)")
 for _b in (1, 8, 32, 64):
     for _c in (512, 2048, 8192):
         WORKLOADS.setdefault(f"decode_{_b}x{_c}", ("decode_uniform", {"batch": _b, "ctx": _c},
@@ -260,7 +262,12 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     builder, kw, desc = WORKLOADS[args.workload]
-    p = getattr(workloads, builder)(device=dev, **kw)
+    if builder == "make_problem_uniform_gqa8":
+        import numpy as _np
+        p = workloads.make_problem("gqa8_uniform", 32, 4, 128, 16, _np.full(64, 4096), 1,
+                                   64 * 256, workloads.BASE_SEED + 3, device=dev)
+    else:
+        p = getattr(workloads, builder)(device=dev, **kw)
     decode_bytes, append_bytes = step_bytes(p)
     rows_per_kv = p.q_len * p.Hq // p.Hkv
     S = args.num_splits if args.num_splits > 0 else lib.choose_num_splits(
