@@ -232,7 +232,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkvqk", choices=["pkvqk", "reference"])
     ap.add_argument("--workload", default="decode_64x8192", choices=sorted(WORKLOADS))
-    ap.add_argument("--num-splits", type=int, default=-1, help="-1: host heuristic")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="0: balanced persistent schedule; -1: split heuristic; >0: fixed splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-seqs", type=int, default=4096)
@@ -270,14 +271,10 @@ def main():
         p = getattr(workloads, builder)(device=dev, **kw)
     decode_bytes, append_bytes = step_bytes(p)
     rows_per_kv = p.q_len * p.Hq // p.Hkv
-    S = args.num_splits if args.num_splits > 0 else lib.choose_num_splits(
+    S = args.num_splits if args.num_splits >= 0 else lib.choose_num_splits(
         p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
     ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    rows = p.B * p.q_len * p.Hq
-    ws_f = ws.view(torch.float32)
-    ws_o = ws_f[: rows * S * 128] if S > 1 else None
-    ws_lse = ws_f[rows * S * 128: rows * S * 129] if S > 1 else None
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if ws_bytes else None
     out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev)
     q = p.q.clone()
     stream = torch.cuda.current_stream()
@@ -285,15 +282,9 @@ def main():
     big_inputs = decode_bytes > 4 * l2_bytes
     flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
 
-    def decode_only():
-        if S > 1:
-            lib.paged_decode_partials(q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, ws,
-                                      q_len=p.q_len, num_splits=S,
-                                      max_seq_len_hint=p.max_seq_len, stream=stream)
-        else:
-            lib.paged_decode(q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
-                             q_len=p.q_len, num_splits=1, max_seq_len_hint=p.max_seq_len,
-                             stream=stream)
+    def decode_call(qq, bt, sl):
+        lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len, num_splits=S,
+                         max_seq_len_hint=p.max_seq_len, workspace=ws, stream=stream)
 
     def step(ev=None):
         if ev is not None:
@@ -302,13 +293,11 @@ def main():
                              p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        decode_only()
+        decode_call(q, p.block_tables, p.seq_lens)
         if ev is not None:
             ev[2].record(stream)
-        if S > 1:
-            lib.lse_combine(ws_o, ws_lse, rows, S, out, stream=stream)
 
-    launches_per_step = 2 + (1 if S > 1 else 0)
+    launches_per_step = 2 + (1 if S != 1 else 0)     # append, decode, combine
 
     for _ in range(args.warmup):
         step()
@@ -361,11 +350,7 @@ def main():
         lib.norm_rope_append(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["positions"],
                              dev_in["slot_mapping"], p.gamma_q, p.gamma_k, p.theta, p.eps,
                              p.k_cache, p.v_cache, stream=stream)
-        nb = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
-        lib.paged_decode(dev_in["q"], p.k_cache, p.v_cache, dev_in["block_tables"],
-                         dev_in["seq_lens"], out, q_len=p.q_len, num_splits=S,
-                         max_seq_len_hint=p.max_seq_len, workspace=ws if nb else None,
-                         stream=stream)
+        decode_call(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"])
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -411,7 +396,8 @@ def main():
             "workload": desc,
             "batch": p.B, "ctx_max": p.max_seq_len, "total_tokens": p.total_tokens,
             "q_len": p.q_len, "heads_q": p.Hq, "heads_kv": p.Hkv, "head_dim": p.D,
-            "block_size": p.block_size, "num_splits": S,
+            "block_size": p.block_size,
+            "schedule": "balanced (one CTA per SM)" if S == 0 else f"split x{S}",
             "l2": ("inputs larger than L2: %.2f GB of K/V per step vs %d MB L2" %
                    (decode_bytes / 1e9, l2_bytes >> 20)) if big_inputs else
                   "L2 flushed (2x L2 write) before every step, excluded from timing",
@@ -423,7 +409,8 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": K * launches_per_step,
         "roofline": {
-            "kernel": "paged_decode_kernel",
+            "kernel": "pkvqk_paged_decode call: paged_decode_kernel"
+                      + ("" if S == 1 else " + its combine kernel"),
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": peak,

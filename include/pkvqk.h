@@ -145,10 +145,14 @@ PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
                                 int32_t sm_count);
 
 /*
- * Workspace bytes pkvqk_paged_decode needs: 0 when num_splits == 1, else
- * batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up to 256.
- * Layout: fp32 partial outputs [rows][num_splits][head_dim] followed by
- * fp32 partial lse [rows][num_splits], rows = (b*q_len + t)*Hq + h.
+ * Workspace bytes pkvqk_paged_decode needs on the current device:
+ * - num_splits == 1: 0;
+ * - num_splits >= 2: batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up to
+ *   256.  Layout: fp32 partial outputs [rows][num_splits][head_dim] followed
+ *   by fp32 partial lse [rows][num_splits], rows = (b*q_len + t)*Hq + h;
+ * - num_splits == 0 (balanced): an upper bound for any kv-head count,
+ *   ((SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded up, where
+ *   SMs is the current device's multiprocessor count (internal layout).
  */
 PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
                                     int32_t num_q_heads, int32_t head_dim,
@@ -166,23 +170,31 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   out = sum_n softmax(s)_n V_n,  lse = log sum_n exp(s_n)
  * A row with no visible key outputs 0 and lse = -inf.
  *
- * Splits: with C = ceil(ceil(max_seq_len_hint / block_size) / num_splits)
- * pages, split j < S-1 of a sequence covers pages [j*C, (j+1)*C) and split
- * S-1 covers [(S-1)*C, end), so every key is covered whatever the hint.
- * Each split keeps an online softmax; for num_splits > 1 the partials go to
- * the workspace and pkvqk_lse_combine merges them (launched by this call).
+ * Schedules (the result does not depend on them, up to rounding):
+ * - num_splits >= 1 (split-KV): with C = ceil(ceil(max_seq_len_hint /
+ *   block_size) / num_splits) pages, split j < S-1 of a sequence covers pages
+ *   [j*C, (j+1)*C) and split S-1 covers [(S-1)*C, end), so every key is
+ *   covered whatever the hint.  Each split keeps an online softmax; for
+ *   num_splits > 1 the partials go to the workspace and the LSE combine
+ *   (launched by this call) merges them.  pkvqk_choose_num_splits gives a
+ *   host-side choice of S.
+ * - num_splits == 0 (balanced): one CTA per SM; the pages of all (sequence,
+ *   kv-head group) pairs are laid end to end and every CTA takes an equal
+ *   contiguous share, crossing sequence boundaries; a sequence covered by one
+ *   CTA is written directly, one cut across CTAs is merged by a combine
+ *   kernel this call launches.  Balances any mix of lengths.
  *
  *   q             device bf16, element (b*q_len + t, h, d) at
  *                 q[(b*q_len + t)*q_stride_t + h*q_stride_h + d]
  *   block_tables  device int32 [batch, max_blocks_per_seq]
  *   seq_lens      device int32 [batch], counting the q_len new tokens
- *   num_splits    1..256, or 0 = pkvqk_choose_num_splits(batch, Hkv,
- *                 q_len*Hq/Hkv, hint, batch*hint, block_size, 0) with hint
- *                 the effective max_seq_len_hint (size the workspace for it)
+ *   num_splits    0 (balanced schedule) or 1..256 (split schedule)
  *   max_seq_len_hint  host int >= the longest seq_len (0 = max_blocks_per_seq*block_size)
  *   out           device bf16 [batch, q_len, Hq, head_dim], contiguous
  *   lse_out       device fp32 [batch, q_len, Hq] or NULL
- *   workspace     device, >= pkvqk_decode_workspace_bytes(...) (NULL if 0)
+ *   workspace     device, >= pkvqk_decode_workspace_bytes(batch, q_len, Hq,
+ *                 head_dim, num_splits) on the current device (NULL if 0);
+ *                 contents need no initialisation
  * Supported: head_dim 128, Hq % Hkv == 0, q_len*Hq/Hkv <= 16.
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode(
@@ -219,7 +231,9 @@ PKVQK_API pkvqk_status pkvqk_paged_decode_partials(
  * allocate — and so cannot pass the split workspace.
  *
  * Same arguments and results as pkvqk_paged_decode minus workspace and
- * workspace_bytes.  The split partials go to a fixed 16 MiB array inside the
+ * workspace_bytes, except that num_splits == 0 here picks the split count
+ * with pkvqk_choose_num_splits (the split schedule) instead of the balanced
+ * schedule.  The split partials go to a fixed 16 MiB array inside the
  * library (pkvqk_static_workspace_capacity()), held on every GPU that loads
  * the library until the process exits.  A call whose partials need more
  * (pkvqk_decode_workspace_bytes for its split count) returns

@@ -148,6 +148,16 @@ int sm_count_current() {
   return n;
 }
 
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// Balanced schedule: fp32 partials [slot rows][128] + lse [slot rows], then
+// the int2 unit table [units].
+size_t balanced_bytes(int64_t slot_rows, int64_t units) {
+  const size_t raw = align16(static_cast<size_t>(slot_rows) * 129 * 4) +
+                     static_cast<size_t>(units) * 8;
+  return (raw + 255) & ~size_t(255);
+}
+
 // Bytes of the fp32 partials [rows][S][128] + partial lse [rows][S].
 size_t partial_bytes(int64_t rows, int S) {
   const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
@@ -200,16 +210,20 @@ pkvqk_status run_decode(const DecodeCall& c) {
   const int hint = c.max_seq_len_hint > 0
                        ? c.max_seq_len_hint
                        : static_cast<int>(std::min<int64_t>(cap_tokens, INT32_MAX));
-  int S = c.num_splits;
-  if (S == 0)
-    S = pkvqk_choose_num_splits(c.batch, L.num_kv_heads, rows, hint,
-                                static_cast<int64_t>(hint) * c.batch, L.block_size, 0);
+  const int S = c.num_splits;                   // 0: balanced schedule
+  const pkvqk::DecodePlan plan = pkvqk::plan_decode(L.num_kv_heads, rows);
   const int64_t nrows = static_cast<int64_t>(c.batch) * c.q_len * c.num_q_heads;
-  const bool use_ws = c.partials_only || S > 1;
-  const size_t need_exact = use_ws ? partial_bytes(nrows, S) : 0;
-  if (use_ws && c.workspace_bytes < need_exact)
+  const int grid_ctas = sm_count_current();
+  const int groups = L.num_kv_heads / plan.heads_per_cta;
+  const int64_t units = static_cast<int64_t>(c.batch) * groups;
+  const int64_t rows_per_unit = static_cast<int64_t>(c.q_len) * plan.heads_per_cta * group;
+  const int64_t slot_rows = (grid_ctas + units) * rows_per_unit;
+  size_t need = 0;
+  if (S == 0) need = balanced_bytes(slot_rows, units);
+  else if (c.partials_only || S > 1) need = partial_bytes(nrows, S);
+  if (need > 0 && c.workspace_bytes < need)
     return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
-                c.workspace_bytes, need_exact);
+                c.workspace_bytes, need);
   if (c.batch == 0) return ok();
 
   PKVQK_TRY(check_device_ptr(c.q, "q"));
@@ -225,13 +239,12 @@ pkvqk_status run_decode(const DecodeCall& c) {
     if (!aligned16(c.out)) return fail(PKVQK_ERR_INVALID_ARG, "out not 16-byte aligned");
     if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
   }
-  if (use_ws) {
+  if (need > 0) {
     PKVQK_TRY(check_device_ptr(c.workspace, "workspace"));
     if (!aligned16(c.workspace)) return fail(PKVQK_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   }
   if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
 
-  const pkvqk::DecodePlan plan = pkvqk::plan_decode(L.num_kv_heads, rows);
   CUtensorMap kmap, vmap;
   PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta));
   PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta));
@@ -252,18 +265,33 @@ pkvqk_status run_decode(const DecodeCall& c) {
   a.block_size = L.block_size;
   a.num_blocks = L.num_blocks;
   a.num_splits = S;
-  a.chunk_pages = std::max(1, (hint_pages + S - 1) / S);
+  a.chunk_pages = S > 0 ? std::max(1, (hint_pages + S - 1) / S) : 0;
+  a.groups = groups;
+  a.rows_per_unit = static_cast<int32_t>(rows_per_unit);
   const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(128.0f);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(c.out);
   a.lse_out = c.lse_out;
-  a.ws_o = use_ws ? static_cast<float*>(c.workspace) : nullptr;
-  a.ws_lse = use_ws ? static_cast<float*>(c.workspace) + nrows * S * 128 : nullptr;
+  a.ws_o = nullptr;
+  a.ws_lse = nullptr;
+  a.unit_info = nullptr;
+  if (S == 0) {
+    a.ws_o = static_cast<float*>(c.workspace);
+    a.ws_lse = a.ws_o + slot_rows * 128;
+    a.unit_info = reinterpret_cast<int2*>(static_cast<char*>(c.workspace) +
+                                          align16(static_cast<size_t>(slot_rows) * 129 * 4));
+  } else if (need > 0) {
+    a.ws_o = static_cast<float*>(c.workspace);
+    a.ws_lse = a.ws_o + nrows * S * 128;
+  }
   a.status_flags = c.status_flags;
 
-  cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, c.stream);
+  cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, grid_ctas, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
-  if (S > 1 && !c.partials_only) {
+  if (S == 0) {
+    e = pkvqk::launch_balanced_combine(a, plan.heads_per_cta, c.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
+  } else if (S > 1 && !c.partials_only) {
     e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
                                   c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
@@ -389,7 +417,16 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
 
 size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_q_heads,
                                     int32_t head_dim, int32_t num_splits) {
-  if (batch <= 0 || q_len <= 0 || num_q_heads <= 0 || head_dim != 128 || num_splits <= 1) return 0;
+  if (batch <= 0 || q_len <= 0 || num_q_heads <= 0 || head_dim != 128 || num_splits == 1 ||
+      num_splits < 0)
+    return 0;
+  if (num_splits == 0) {
+    // bound over every kv-head count: slots (SMs + units) x rows per unit
+    // <= (SMs + batch) x q_len x Hq, units <= batch x Hq
+    const int64_t per = static_cast<int64_t>(q_len) * num_q_heads;
+    return balanced_bytes((sm_count_current() + static_cast<int64_t>(batch)) * per,
+                          static_cast<int64_t>(batch) * num_q_heads);
+  }
   return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits);
 }
 

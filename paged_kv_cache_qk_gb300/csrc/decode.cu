@@ -7,17 +7,29 @@
 // FlashAttention BSHD cache through strided views) and item 4 (one verify
 // forward over k+1 tokens per sequence, causal among the draft tokens).
 //
-// Work decomposition: one CTA per (split, group of HPC kv heads, sequence).
-// Warp HPC is the producer: its lanes fetch 32 block-table entries at a time
-// and lane 0 issues, per 16-key tile, one 5-D TMA box for K and one for V
-// (HPC heads x 16 slots x 128 dims each, 128-byte swizzled) into a ring of
-// STAGES shared-memory stages guarded by full/empty mbarriers.  Warps
-// 0..HPC-1 are consumers, one per kv head; each handles every q row that
-// reads its kv head (rows = q_len * group):
+// A CTA owns HPC kv heads ("head group") of some sequences and walks a list
+// of segments — runs of 16-key tiles of one (sequence, head group).  Two
+// schedules produce the segment list:
+//   * split   (num_splits >= 1): grid (S, head groups, batch), one segment
+//     per CTA: split j of the sequence (chunk_pages pages per split, the last
+//     split takes the rest);
+//   * balanced (num_splits == 0): a persistent grid of one CTA per SM; the
+//     pages of all (head group, sequence) units are laid end to end and CTA c
+//     takes pages [c*TP/G, (c+1)*TP/G) of that list, crossing sequence
+//     boundaries without refilling its pipeline.  A unit that one CTA covers
+//     whole is written straight to the output; a unit cut across CTAs leaves
+//     one partial per CTA in slot (cta + unit), merged by the combine kernel.
+// Warp HPC is the producer: it walks the same segment list, its lanes fetch
+// 32 block-table entries at a time and lane 0 issues, per 16-key tile, one
+// 5-D TMA box for K and one for V (HPC heads x 16 slots x 128 dims each,
+// 128-byte swizzled) into a ring of STAGES shared-memory stages guarded by
+// full/empty mbarriers; the ring runs on across segments.  Warps 0..HPC-1
+// consume, one per kv head, every q row that reads their kv head
+// (rows = q_len * group):
 //   * rows <= 4 ("simt"): 8 lanes per key, 4 keys per warp instruction; each
 //     lane holds 16 of the 128 dims, the q.k dot is a 3-step xor-shuffle
 //     reduction; every 8-lane key group keeps its own online softmax and the
-//     four groups are merged by shuffles after the last tile.
+//     four groups are merged by shuffles at the end of a segment.
 //   * rows 5..16 ("tc"): the 16 padded rows x 16 keys score tile and the
 //     16 rows x 128 dims output tile are mma.sync m16n8k16 bf16 contractions
 //     fed by ldmatrix from the swizzled stages (conflict-free).
@@ -43,31 +55,193 @@ struct Geometry {
   static constexpr int kThreads = (HPC + 1) * 32;
 };
 
-struct SplitRange {
-  int k0, k1, ntiles, seq_len;
+constexpr int kDestFinal = 0;   // bf16 output + lse
+constexpr int kDestSplit = 1;   // partial at [row][split] (split schedule)
+constexpr int kDestSlot = 2;    // partial at [slot][row in unit] (balanced schedule)
+
+// A run of 16-key tiles of one (sequence, head group): keys [k0, k1).
+struct Segment {
+  int b, hg, seq_len, k0, k1, ntiles, dest, split;
+  long long slot;
 };
 
-// Key range [k0, k1) of split `split` of sequence b (partition: chunk_pages
-// pages per split, the last split takes the remainder).
-__device__ __forceinline__ SplitRange split_range(const DecodeArgs& a, int b, int split) {
-  SplitRange r;
+__device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b) {
   int L = a.seq_lens[b];
   if (L < 0) L = 0;
-  const int64_t cap = static_cast<int64_t>(a.max_blocks_per_seq) * a.block_size;
+  const long long cap = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
   if (L > cap) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) report(a.status_flags, kFlagBadBlock);
+    report(a.status_flags, kFlagBadBlock);
     L = static_cast<int>(cap);
   }
-  const int P = (L + a.block_size - 1) / a.block_size;
-  int p0 = split * a.chunk_pages;
-  int p1 = (split == a.num_splits - 1) ? P : p0 + a.chunk_pages;
-  p0 = min(p0, P);
-  p1 = min(p1, P);
-  r.seq_len = L;
-  r.k0 = p0 * a.block_size;
-  r.k1 = min(p1 * a.block_size, L);
-  r.ntiles = r.k1 > r.k0 ? (r.k1 - r.k0 + kTileKeys - 1) / kTileKeys : 0;
-  return r;
+  return L;
+}
+
+__device__ __forceinline__ long long unit_pages(const DecodeArgs& a, int u) {
+  const int L = clamped_len(a, u % a.batch);
+  return (L + a.block_size - 1) / a.block_size;
+}
+
+__device__ __forceinline__ void set_range(Segment& s, int k0, int k1) {
+  s.k0 = k0;
+  s.k1 = k1;
+  s.ntiles = k1 > k0 ? (k1 - k0 + kTileKeys - 1) / kTileKeys : 0;
+}
+
+// Balanced schedule of this CTA: its page range and where its walk starts.
+struct Plan {
+  long long tp, lo, hi;     // total pages; this CTA's pages [lo, hi)
+  int u_start;              // first unit with pages at or after lo
+  long long s_start;        // pages before unit u_start
+};
+
+// Produces the CTA's segments in order; producer and consumers each run
+// their own copy and see the same sequence.
+struct SegmentSource {
+  const DecodeArgs* a;
+  const Plan* plan;
+  int balanced;
+  int done;
+  int u;
+  long long s;              // pages before unit u
+
+  __device__ void init(const DecodeArgs& args, const Plan* p) {
+    a = &args;
+    plan = p;
+    balanced = args.num_splits == 0;
+    done = 0;
+    u = 0;
+    s = 0;
+    if (balanced) {
+      u = p->u_start;
+      s = p->s_start;
+    }
+  }
+
+  __device__ bool next(Segment& seg) {
+    if (!balanced) {
+      if (done) return false;
+      done = 1;
+      seg.b = blockIdx.z;
+      seg.hg = blockIdx.y;
+      seg.split = blockIdx.x;
+      seg.slot = 0;
+      seg.seq_len = clamped_len(*a, seg.b);
+      const int P = (seg.seq_len + a->block_size - 1) / a->block_size;
+      int p0 = seg.split * a->chunk_pages;
+      int p1 = (seg.split == a->num_splits - 1) ? P : p0 + a->chunk_pages;
+      p0 = min(p0, P);
+      p1 = min(p1, P);
+      set_range(seg, p0 * a->block_size, min(p1 * a->block_size, seg.seq_len));
+      seg.dest = a->num_splits == 1 ? kDestFinal : kDestSplit;
+      return true;
+    }
+    const int U = a->batch * a->groups;
+    while (u < U && s < plan->hi) {
+      const int cur = u;
+      const long long start = s;
+      const long long P = unit_pages(*a, cur);
+      u += 1;
+      s += P;
+      const long long plo = max(start, plan->lo) - start;
+      const long long phi = min(s, plan->hi) - start;
+      if (phi <= plo) continue;                            // empty unit or no overlap
+      seg.b = cur % a->batch;
+      seg.hg = cur / a->batch;
+      seg.split = 0;
+      seg.seq_len = clamped_len(*a, seg.b);
+      set_range(seg, static_cast<int>(plo) * a->block_size,
+                min(static_cast<int>(phi) * a->block_size, seg.seq_len));
+      const bool whole = plo == 0 && phi == P;
+      seg.dest = whole ? kDestFinal : kDestSlot;
+      seg.slot = static_cast<long long>(blockIdx.x) + cur;
+      // the CTA holding the unit's first page records which CTAs cut it:
+      // page x belongs to CTA floor(((x + 1) * G - 1) / TP)
+      if (start >= plan->lo && threadIdx.x == 0) {
+        const long long G = gridDim.x;
+        const int c_last = static_cast<int>((s * G - 1) / plan->tp);
+        a->unit_info[cur] = make_int2(blockIdx.x, c_last);
+      }
+      return true;
+    }
+    return false;
+  }
+};
+
+// Block-wide plan of the balanced schedule (every thread takes part).
+__device__ void make_plan(const DecodeArgs& a, Plan* plan, long long* wsum) {
+  const int U = a.batch * a.groups;
+  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = nt >> 5;
+  const int chunk = (U + nt - 1) / nt;
+  const int u_lo = min(U, tid * chunk), u_hi = min(U, u_lo + chunk);
+  long long mine = 0;
+  for (int u = u_lo; u < u_hi; ++u) mine += unit_pages(a, u);
+  long long v = mine;                                       // inclusive warp scan
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) wsum[warp] = v;
+  if (tid == 0) plan->u_start = U;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nwarps ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < nwarps) wsum[lane] = w;
+  }
+  __syncthreads();
+  const long long tp = wsum[nwarps - 1];
+  const long long before = (warp ? wsum[warp - 1] : 0) + v - mine;   // pages before u_lo
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long lo = c * tp / G, hi = (c + 1) * tp / G;
+  long long run = before;
+  for (int u = u_lo; u < u_hi; ++u) {
+    const long long P = unit_pages(a, u);
+    if (run + P > lo) {
+      atomicMin(&plan->u_start, u);
+      break;
+    }
+    run += P;
+  }
+  __syncthreads();
+  run = before;
+  for (int u = u_lo; u < u_hi; ++u) {
+    if (u == plan->u_start) plan->s_start = run;
+    run += unit_pages(a, u);
+  }
+  if (tid == 0) {
+    plan->tp = tp;
+    plan->lo = lo;
+    plan->hi = hi;
+    if (plan->u_start == U) plan->s_start = tp;
+  }
+  __syncthreads();
+}
+
+// Units without any key: zero output, lse -inf, nothing to combine.  Unit u
+// is handled by CTA u mod G (all threads of the CTA).
+__device__ void write_empty_units(const DecodeArgs& a, int hpc) {
+  const int U = a.batch * a.groups;
+  for (int u = blockIdx.x; u < U; u += gridDim.x) {
+    if (unit_pages(a, u) != 0) continue;
+    const int b = u % a.batch, hg = u / a.batch;
+    const int rows = a.rows_per_unit;
+    for (int idx = threadIdx.x; idx < rows * (kHeadDim / 8); idx += blockDim.x) {
+      const int r = idx / (kHeadDim / 8), c8 = idx % (kHeadDim / 8);
+      // unit row r = (t * HPC + hh) * group + gi
+      const int gi = r % a.group, th = r / a.group, hh = th % hpc, t = th / hpc;
+      const int h = (hg * hpc + hh) * a.group + gi;
+      const long long row = (static_cast<long long>(b) * a.q_len + t) * a.num_q_heads + h;
+      *reinterpret_cast<uint4*>(a.out + row * kHeadDim + c8 * 8) = make_uint4(0, 0, 0, 0);
+      if (c8 == 0 && a.lse_out != nullptr) a.lse_out[row] = -INFINITY;
+    }
+    if (threadIdx.x == 0) a.unit_info[u] = make_int2(blockIdx.x, blockIdx.x);
+  }
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -79,8 +253,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 template <int HPC, int STAGES>
 __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& a,
-                        int b, int hg, const SplitRange& r, uint8_t* stages, uint64_t* full,
-                        uint64_t* empty, volatile int* abort_flag, int* issued_out) {
+                        const Plan* plan, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                        volatile int* abort_flag, int* issued_out) {
   constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -88,48 +262,53 @@ __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const 
     prefetch_tensormap(vmap);
   }
   const uint64_t pol = l2_evict_first_policy();
-  const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-  int issued = 0;
+  SegmentSource src;
+  src.init(a, plan);
+  Segment seg;
+  int it = 0;                      // tiles issued so far (ring position)
   bool ok = true;
-  for (int i0 = 0; i0 < r.ntiles && ok; i0 += 32) {
-    int blk = 0, slot0 = 0;
-    const int i = i0 + lane;
-    if (i < r.ntiles) {
-      const int key = r.k0 + i * kTileKeys;
-      const int page = key / a.block_size;
-      slot0 = key - page * a.block_size;
-      blk = __ldg(bt + page);
-      if (blk < 0 || blk >= a.num_blocks) report(a.status_flags, kFlagBadBlock);
-    }
-    const int n = min(32, r.ntiles - i0);
-    for (int j = 0; j < n; ++j) {
-      const int bj = __shfl_sync(0xffffffffu, blk, j);
-      const int sj = __shfl_sync(0xffffffffu, slot0, j);
-      int good = 1;
-      if (lane == 0) {
-        const int it = i0 + j;
-        const int s = it % STAGES;
-        if (it >= STAGES) good = mbar_wait(&empty[s], ((it / STAGES) - 1) & 1) ? 1 : 0;
-        if (good) {
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          uint8_t* dst = stages + s * kStageBytes;
-          // coordinates: (dim lo, slot, dim half, kv head, block)
-          tma_load_5d(dst, kmap, &full[s], 0, sj, 0, hg * HPC, bj, pol);
-          tma_load_5d(dst + HPC * kHeadTileBytes, vmap, &full[s], 0, sj, 0, hg * HPC, bj, pol);
-          issued = it + 1;
-        } else {
-          *abort_flag = 1;
-          report(a.status_flags, kFlagTimeout);
-        }
+  while (ok && src.next(seg)) {
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(seg.b) * a.max_blocks_per_seq;
+    for (int i0 = 0; i0 < seg.ntiles && ok; i0 += 32) {
+      int blk = 0, slot0 = 0;
+      const int i = i0 + lane;
+      if (i < seg.ntiles) {
+        const int key = seg.k0 + i * kTileKeys;
+        const int page = key / a.block_size;
+        slot0 = key - page * a.block_size;
+        blk = __ldg(bt + page);
+        if (blk < 0 || blk >= a.num_blocks) report(a.status_flags, kFlagBadBlock);
       }
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) {
-        ok = false;
-        break;
+      const int n = min(32, seg.ntiles - i0);
+      for (int j = 0; j < n; ++j) {
+        const int bj = __shfl_sync(0xffffffffu, blk, j);
+        const int sj = __shfl_sync(0xffffffffu, slot0, j);
+        int good = 1;
+        if (lane == 0) {
+          const int s = it % STAGES;
+          if (it >= STAGES) good = mbar_wait(&empty[s], ((it / STAGES) - 1) & 1) ? 1 : 0;
+          if (good) {
+            mbar_arrive_expect_tx(&full[s], kStageBytes);
+            uint8_t* dst = stages + s * kStageBytes;
+            // coordinates: (dim lo, slot, dim half, kv head, block)
+            tma_load_5d(dst, kmap, &full[s], 0, sj, 0, seg.hg * HPC, bj, pol);
+            tma_load_5d(dst + HPC * kHeadTileBytes, vmap, &full[s], 0, sj, 0, seg.hg * HPC, bj,
+                        pol);
+          } else {
+            *abort_flag = 1;
+            report(a.status_flags, kFlagTimeout);
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        ++it;
       }
     }
   }
-  if (lane == 0) *issued_out = issued;
+  if (lane == 0) *issued_out = it;
 }
 
 // After a timeout: wait (bounded) for the last copy issued into every stage
@@ -143,12 +322,32 @@ __device__ void drain(uint64_t* full, int issued) {
   }
 }
 
-// ------------------------------------------------------- output of a split
+// -------------------------------------------------------- row destinations
 
-// Writes one row's result: bf16 output + lse when there is one split,
-// otherwise fp32 partial + partial lse into the workspace.
-__device__ __forceinline__ int64_t out_row(const DecodeArgs& a, int b, int t, int h) {
-  return (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
+struct RowDest {
+  __nv_bfloat16* out;   // final bf16 row (or null)
+  float* lse;           // final lse (or null)
+  float* po;            // partial fp32 row (or null)
+  float* plse;          // partial lse (or null)
+};
+
+template <int HPC>
+__device__ __forceinline__ RowDest row_dest(const DecodeArgs& a, const Segment& seg, int t,
+                                            int hh, int gi) {
+  RowDest d{nullptr, nullptr, nullptr, nullptr};
+  const int h = (seg.hg * HPC + hh) * a.group + gi;
+  const long long row = (static_cast<long long>(seg.b) * a.q_len + t) * a.num_q_heads + h;
+  if (seg.dest == kDestFinal) {
+    d.out = a.out + row * kHeadDim;
+    d.lse = a.lse_out != nullptr ? a.lse_out + row : nullptr;
+  } else {
+    const long long idx = seg.dest == kDestSplit
+                              ? row * a.num_splits + seg.split
+                              : seg.slot * a.rows_per_unit + (t * HPC + hh) * a.group + gi;
+    d.po = a.ws_o + idx * kHeadDim;
+    d.plse = a.ws_lse + idx;
+  }
+  return d;
 }
 
 __device__ __forceinline__ float final_lse(float m, float l) {
@@ -158,154 +357,165 @@ __device__ __forceinline__ float final_lse(float m, float l) {
 // ------------------------------------------------------ CUDA-core consumer
 
 template <int HPC, int STAGES, int R>
-__device__ void consume_simt(const DecodeArgs& a, int b, int split, int hg, const SplitRange& r,
-                             const uint8_t* stages, uint64_t* full, uint64_t* empty,
-                             volatile int* abort_flag) {
+__device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_t* stages,
+                             uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
   const int lane = threadIdx.x & 31;
   const int hh = threadIdx.x >> 5;
-  const int kvh = hg * HPC + hh;
-  const int kg = lane >> 3;        // key group: key 4*it + kg of the tile
+  const int kg = lane >> 3;        // key group: key 4*q4 + kg of the tile
   const int p = lane & 7;          // 16-byte chunk p of each 64-dim half
 
-  float qf[R][16], acc[R][16], m[R], l[R];
-  int limit[R];
+  SegmentSource src;
+  src.init(a, plan);
+  Segment seg;
+  int it = 0;                      // tiles consumed so far (ring position)
+  bool aborted = false;
+  while (!aborted && src.next(seg)) {
+    const int kvh = seg.hg * HPC + hh;
+    float qf[R][16], acc[R][16], m[R], l[R];
+    int limit[R];
 #pragma unroll
-  for (int rr = 0; rr < R; ++rr) {
-    const int t = rr / a.group, gi = rr - t * a.group;
-    const __nv_bfloat16* qrow = a.q + (static_cast<int64_t>(b) * a.q_len + t) * a.q_stride_t +
-                                static_cast<int64_t>(kvh * a.group + gi) * a.q_stride_h;
-    const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * p));
-    const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(qrow + 64 + 8 * p));
-    unpack8(u0, qf[rr]);
-    unpack8(u1, qf[rr] + 8);
+    for (int rr = 0; rr < R; ++rr) {
+      const int t = rr / a.group, gi = rr - t * a.group;
+      const __nv_bfloat16* qrow = a.q +
+                                  (static_cast<int64_t>(seg.b) * a.q_len + t) * a.q_stride_t +
+                                  static_cast<int64_t>(kvh * a.group + gi) * a.q_stride_h;
+      const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * p));
+      const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(qrow + 64 + 8 * p));
+      unpack8(u0, qf[rr]);
+      unpack8(u1, qf[rr] + 8);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      qf[rr][j] *= a.scale_log2;
-      acc[rr][j] = 0.f;
+      for (int j = 0; j < 16; ++j) {
+        qf[rr][j] *= a.scale_log2;
+        acc[rr][j] = 0.f;
+      }
+      m[rr] = -INFINITY;
+      l[rr] = 0.f;
+      limit[rr] = seg.seq_len - a.q_len + t + 1;
     }
-    m[rr] = -INFINITY;
-    l[rr] = 0.f;
-    limit[rr] = r.seq_len - a.q_len + t + 1;
-  }
 
-  for (int i = 0; i < r.ntiles; ++i) {
-    const int s = i % STAGES;
-    if (!mbar_wait(&full[s], (i / STAGES) & 1)) {
-      *abort_flag = 1;
-      report(a.status_flags, kFlagTimeout);
-      break;
-    }
-    const uint8_t* kt = stages + s * kStageBytes + hh * kHeadTileBytes;
-    const uint8_t* vt = kt + HPC * kHeadTileBytes;
-    const int key0 = r.k0 + i * kTileKeys;
+    for (int i = 0; i < seg.ntiles; ++i, ++it) {
+      const int s = it % STAGES;
+      if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
+        *abort_flag = 1;
+        report(a.status_flags, kFlagTimeout);
+        aborted = true;
+        break;
+      }
+      const uint8_t* kt = stages + s * kStageBytes + hh * kHeadTileBytes;
+      const uint8_t* vt = kt + HPC * kHeadTileBytes;
+      const int key0 = seg.k0 + i * kTileKeys;
 
-    float sc[R][4];
+      float sc[R][4];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int row = it * 4 + kg;
-      const uint4 k0 = *reinterpret_cast<const uint4*>(kt + swz128(row, p));
-      const uint4 k1 = *reinterpret_cast<const uint4*>(kt + kHalfTileBytes + swz128(row, p));
-      float kf[16];
-      unpack8(k0, kf);
-      unpack8(k1, kf + 8);
-      const int n = key0 + row;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int row = q4 * 4 + kg;
+        const uint4 k0 = *reinterpret_cast<const uint4*>(kt + swz128(row, p));
+        const uint4 k1 = *reinterpret_cast<const uint4*>(kt + kHalfTileBytes + swz128(row, p));
+        float kf[16];
+        unpack8(k0, kf);
+        unpack8(k1, kf + 8);
+        const int n = key0 + row;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+          float d = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) d = fmaf(qf[rr][j], kf[j], d);
+          d += __shfl_xor_sync(0xffffffffu, d, 4);
+          d += __shfl_xor_sync(0xffffffffu, d, 2);
+          d += __shfl_xor_sync(0xffffffffu, d, 1);
+          sc[rr][q4] = (n < limit[rr]) ? d : -INFINITY;
+        }
+      }
+
+      float pr[R][4];
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
-        float d = 0.f;
+        const float mt = fmaxf(fmaxf(sc[rr][0], sc[rr][1]), fmaxf(sc[rr][2], sc[rr][3]));
+        const float mn = fmaxf(m[rr], mt);
+        const float mu = (mn == -INFINITY) ? 0.f : mn;
+        const float alpha = exp2f(m[rr] - mu);
+        m[rr] = mn;
+        float ls = l[rr] * alpha;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) d = fmaf(qf[rr][j], kf[j], d);
-        d += __shfl_xor_sync(0xffffffffu, d, 4);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        sc[rr][it] = (n < limit[rr]) ? d : -INFINITY;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          pr[rr][q4] = exp2f(sc[rr][q4] - mu);
+          ls += pr[rr][q4];
+        }
+        l[rr] = ls;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[rr][j] *= alpha;
+      }
+
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int row = q4 * 4 + kg;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(vt + swz128(row, p));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(vt + kHalfTileBytes + swz128(row, p));
+        float vf[16];
+        unpack8(v0, vf);
+        unpack8(v1, vf + 8);
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[rr][j] = fmaf(pr[rr][q4], vf[j], acc[rr][j]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // merge the four key groups (lanes 8 and 16 apart)
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[rr], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[rr], off);
+        const float mn = fmaxf(m[rr], mo);
+        const float mu = (mn == -INFINITY) ? 0.f : mn;
+        const float ea = exp2f(m[rr] - mu), eb = exp2f(mo - mu);
+        l[rr] = l[rr] * ea + lo * eb;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          acc[rr][j] = acc[rr][j] * ea + __shfl_xor_sync(0xffffffffu, acc[rr][j], off) * eb;
+        m[rr] = mn;
       }
     }
 
-    float pr[R][4];
+    if (kg == 0) {
 #pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-      const float mt = fmaxf(fmaxf(sc[rr][0], sc[rr][1]), fmaxf(sc[rr][2], sc[rr][3]));
-      const float mn = fmaxf(m[rr], mt);
-      const float mu = (mn == -INFINITY) ? 0.f : mn;
-      const float alpha = exp2f(m[rr] - mu);
-      m[rr] = mn;
-      float ls = l[rr] * alpha;
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        pr[rr][it] = exp2f(sc[rr][it] - mu);
-        ls += pr[rr][it];
+      for (int rr = 0; rr < R; ++rr) {
+        const int t = rr / a.group, gi = rr - t * a.group;
+        const RowDest d = row_dest<HPC>(a, seg, t, hh, gi);
+        const float inv = l[rr] > 0.f ? 1.f / l[rr] : 0.f;
+        const float lse = final_lse(m[rr], l[rr]);
+        if (d.out != nullptr) {
+          uint4 w0, w1;
+          w0.x = pack_bf16x2(acc[rr][0] * inv, acc[rr][1] * inv);
+          w0.y = pack_bf16x2(acc[rr][2] * inv, acc[rr][3] * inv);
+          w0.z = pack_bf16x2(acc[rr][4] * inv, acc[rr][5] * inv);
+          w0.w = pack_bf16x2(acc[rr][6] * inv, acc[rr][7] * inv);
+          w1.x = pack_bf16x2(acc[rr][8] * inv, acc[rr][9] * inv);
+          w1.y = pack_bf16x2(acc[rr][10] * inv, acc[rr][11] * inv);
+          w1.z = pack_bf16x2(acc[rr][12] * inv, acc[rr][13] * inv);
+          w1.w = pack_bf16x2(acc[rr][14] * inv, acc[rr][15] * inv);
+          *reinterpret_cast<uint4*>(d.out + 8 * p) = w0;
+          *reinterpret_cast<uint4*>(d.out + 64 + 8 * p) = w1;
+          if (p == 0 && d.lse != nullptr) *d.lse = lse;
+        } else {
+          float4* o0 = reinterpret_cast<float4*>(d.po + 8 * p);
+          float4* o1 = reinterpret_cast<float4*>(d.po + 64 + 8 * p);
+          o0[0] = make_float4(acc[rr][0] * inv, acc[rr][1] * inv, acc[rr][2] * inv,
+                              acc[rr][3] * inv);
+          o0[1] = make_float4(acc[rr][4] * inv, acc[rr][5] * inv, acc[rr][6] * inv,
+                              acc[rr][7] * inv);
+          o1[0] = make_float4(acc[rr][8] * inv, acc[rr][9] * inv, acc[rr][10] * inv,
+                              acc[rr][11] * inv);
+          o1[1] = make_float4(acc[rr][12] * inv, acc[rr][13] * inv, acc[rr][14] * inv,
+                              acc[rr][15] * inv);
+          if (p == 0) *d.plse = lse;
+        }
       }
-      l[rr] = ls;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[rr][j] *= alpha;
-    }
-
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int row = it * 4 + kg;
-      const uint4 v0 = *reinterpret_cast<const uint4*>(vt + swz128(row, p));
-      const uint4 v1 = *reinterpret_cast<const uint4*>(vt + kHalfTileBytes + swz128(row, p));
-      float vf[16];
-      unpack8(v0, vf);
-      unpack8(v1, vf + 8);
-#pragma unroll
-      for (int rr = 0; rr < R; ++rr)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[rr][j] = fmaf(pr[rr][it], vf[j], acc[rr][j]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
-
-  // merge the four key groups (lanes 8 and 16 apart)
-#pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
-#pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m[rr], off);
-      const float lo = __shfl_xor_sync(0xffffffffu, l[rr], off);
-      const float mn = fmaxf(m[rr], mo);
-      const float mu = (mn == -INFINITY) ? 0.f : mn;
-      const float ea = exp2f(m[rr] - mu), eb = exp2f(mo - mu);
-      l[rr] = l[rr] * ea + lo * eb;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        acc[rr][j] = acc[rr][j] * ea + __shfl_xor_sync(0xffffffffu, acc[rr][j], off) * eb;
-      m[rr] = mn;
-    }
-  }
-
-  if (kg != 0) return;
-#pragma unroll
-  for (int rr = 0; rr < R; ++rr) {
-    const int t = rr / a.group, gi = rr - t * a.group;
-    const int64_t row = out_row(a, b, t, kvh * a.group + gi);
-    const float inv = l[rr] > 0.f ? 1.f / l[rr] : 0.f;
-    const float lse = final_lse(m[rr], l[rr]);
-    if (a.num_splits == 1) {
-      __nv_bfloat16* o = a.out + row * kHeadDim;
-      uint4 w0, w1;
-      w0.x = pack_bf16x2(acc[rr][0] * inv, acc[rr][1] * inv);
-      w0.y = pack_bf16x2(acc[rr][2] * inv, acc[rr][3] * inv);
-      w0.z = pack_bf16x2(acc[rr][4] * inv, acc[rr][5] * inv);
-      w0.w = pack_bf16x2(acc[rr][6] * inv, acc[rr][7] * inv);
-      w1.x = pack_bf16x2(acc[rr][8] * inv, acc[rr][9] * inv);
-      w1.y = pack_bf16x2(acc[rr][10] * inv, acc[rr][11] * inv);
-      w1.z = pack_bf16x2(acc[rr][12] * inv, acc[rr][13] * inv);
-      w1.w = pack_bf16x2(acc[rr][14] * inv, acc[rr][15] * inv);
-      *reinterpret_cast<uint4*>(o + 8 * p) = w0;
-      *reinterpret_cast<uint4*>(o + 64 + 8 * p) = w1;
-      if (p == 0 && a.lse_out != nullptr) a.lse_out[row] = lse;
-    } else {
-      float* o = a.ws_o + (row * a.num_splits + split) * kHeadDim;
-      float4* o0 = reinterpret_cast<float4*>(o + 8 * p);
-      float4* o1 = reinterpret_cast<float4*>(o + 64 + 8 * p);
-      o0[0] = make_float4(acc[rr][0] * inv, acc[rr][1] * inv, acc[rr][2] * inv, acc[rr][3] * inv);
-      o0[1] = make_float4(acc[rr][4] * inv, acc[rr][5] * inv, acc[rr][6] * inv, acc[rr][7] * inv);
-      o1[0] = make_float4(acc[rr][8] * inv, acc[rr][9] * inv, acc[rr][10] * inv, acc[rr][11] * inv);
-      o1[1] = make_float4(acc[rr][12] * inv, acc[rr][13] * inv, acc[rr][14] * inv, acc[rr][15] * inv);
-      if (p == 0) a.ws_lse[row * a.num_splits + split] = lse;
     }
   }
 }
@@ -336,155 +546,159 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
 }
 
 template <int HPC, int STAGES>
-__device__ void consume_tc(const DecodeArgs& a, int b, int split, int hg, const SplitRange& r,
-                           const uint8_t* stages, uint64_t* full, uint64_t* empty,
-                           volatile int* abort_flag) {
+__device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t* stages,
+                           uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
   const int lane = threadIdx.x & 31;
   const int hh = threadIdx.x >> 5;
-  const int kvh = hg * HPC + hh;
   const int g = lane >> 2;         // fragment row group
   const int c = lane & 3;          // thread in group
   const int R = a.q_len * a.group;
   const int rA = g, rB = g + 8;    // the two q rows this thread's fragments touch
-
-  auto qrow_ptr = [&](int rr) {
-    const int t = rr / a.group, gi = rr - t * a.group;
-    return a.q + (static_cast<int64_t>(b) * a.q_len + t) * a.q_stride_t +
-           static_cast<int64_t>(kvh * a.group + gi) * a.q_stride_h;
-  };
   const bool vA = rA < R, vB = rB < R;
-  const __nv_bfloat16* qA = vA ? qrow_ptr(rA) : a.q;
-  const __nv_bfloat16* qB = vB ? qrow_ptr(rB) : a.q;
-  const int limA = vA ? r.seq_len - a.q_len + rA / a.group + 1 : 0;
-  const int limB = vB ? r.seq_len - a.q_len + rB / a.group + 1 : 0;
-
-  uint32_t qa[8][4];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int d0 = 16 * kk + 2 * c;
-    qa[kk][0] = vA ? __ldg(reinterpret_cast<const uint32_t*>(qA + d0)) : 0u;
-    qa[kk][1] = vB ? __ldg(reinterpret_cast<const uint32_t*>(qB + d0)) : 0u;
-    qa[kk][2] = vA ? __ldg(reinterpret_cast<const uint32_t*>(qA + d0 + 8)) : 0u;
-    qa[kk][3] = vB ? __ldg(reinterpret_cast<const uint32_t*>(qB + d0 + 8)) : 0u;
-  }
-
-  float o[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-
   const int mat = lane >> 3;       // which 8x8 matrix this lane addresses in ldmatrix.x4
   const int mrow = lane & 7;
 
-  for (int i = 0; i < r.ntiles; ++i) {
-    const int s = i % STAGES;
-    if (!mbar_wait(&full[s], (i / STAGES) & 1)) {
-      *abort_flag = 1;
-      report(a.status_flags, kFlagTimeout);
-      break;
-    }
-    const uint32_t kt = smem_addr(stages + s * kStageBytes + hh * kHeadTileBytes);
-    const uint32_t vt = kt + HPC * kHeadTileBytes;
-    const int key0 = r.k0 + i * kTileKeys;
+  SegmentSource src;
+  src.init(a, plan);
+  Segment seg;
+  int it = 0;                      // tiles consumed so far (ring position)
+  bool aborted = false;
+  while (!aborted && src.next(seg)) {
+    const int kvh = seg.hg * HPC + hh;
+    auto qrow_ptr = [&](int rr) {
+      const int t = rr / a.group, gi = rr - t * a.group;
+      return a.q + (static_cast<int64_t>(seg.b) * a.q_len + t) * a.q_stride_t +
+             static_cast<int64_t>(kvh * a.group + gi) * a.q_stride_h;
+    };
+    const __nv_bfloat16* qA = vA ? qrow_ptr(rA) : a.q;
+    const __nv_bfloat16* qB = vB ? qrow_ptr(rB) : a.q;
+    const int limA = vA ? seg.seq_len - a.q_len + rA / a.group + 1 : 0;
+    const int limB = vB ? seg.seq_len - a.q_len + rB / a.group + 1 : 0;
 
-    // S (16 rows x 16 keys) = Q K^T
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    uint32_t qa[8][4];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const int key = ((mat >> 1) << 3) + mrow;
-      const int ch = 2 * kk + (mat & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kt + (ch >> 3) * kHalfTileBytes + swz128(key, ch & 7), b0, b1, b2, b3);
-      mma_bf16(sc[0], qa[kk], b0, b1);
-      mma_bf16(sc[1], qa[kk], b2, b3);
+      const int d0 = 16 * kk + 2 * c;
+      qa[kk][0] = vA ? __ldg(reinterpret_cast<const uint32_t*>(qA + d0)) : 0u;
+      qa[kk][1] = vB ? __ldg(reinterpret_cast<const uint32_t*>(qB + d0)) : 0u;
+      qa[kk][2] = vA ? __ldg(reinterpret_cast<const uint32_t*>(qA + d0 + 8)) : 0u;
+      qa[kk][3] = vB ? __ldg(reinterpret_cast<const uint32_t*>(qB + d0 + 8)) : 0u;
     }
 
+    float o[16][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+
+    for (int i = 0; i < seg.ntiles; ++i, ++it) {
+      const int s = it % STAGES;
+      if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
+        *abort_flag = 1;
+        report(a.status_flags, kFlagTimeout);
+        aborted = true;
+        break;
+      }
+      const uint32_t kt = smem_addr(stages + s * kStageBytes + hh * kHeadTileBytes);
+      const uint32_t vt = kt + HPC * kHeadTileBytes;
+      const int key0 = seg.k0 + i * kTileKeys;
+
+      // S (16 rows x 16 keys) = Q K^T
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = key0 + 8 * nt + 2 * c + (e & 1);
-        const int lim = (e < 2) ? limA : limB;
-        sc[nt][e] = (key < lim) ? sc[nt][e] * a.scale_log2 : -INFINITY;
+      for (int kk = 0; kk < 8; ++kk) {
+        const int key = ((mat >> 1) << 3) + mrow;
+        const int ch = 2 * kk + (mat & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kt + (ch >> 3) * kHalfTileBytes + swz128(key, ch & 7), b0, b1, b2, b3);
+        mma_bf16(sc[0], qa[kk], b0, b1);
+        mma_bf16(sc[1], qa[kk], b2, b3);
       }
 
-    float tA = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    float tB = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-    tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
-    tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
-    tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
-    tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
-    const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-    const float uA = (nA == -INFINITY) ? 0.f : nA;
-    const float uB = (nB == -INFINITY) ? 0.f : nB;
-    const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
-    mA = nA;
-    mB = nB;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sc[nt][0] = exp2f(sc[nt][0] - uA);
-      sc[nt][1] = exp2f(sc[nt][1] - uA);
-      sc[nt][2] = exp2f(sc[nt][2] - uB);
-      sc[nt][3] = exp2f(sc[nt][3] - uB);
-    }
-    lA = lA * alA + (sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]);
-    lB = lB * alB + (sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]);
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      o[nt][0] *= alA;
-      o[nt][1] *= alA;
-      o[nt][2] *= alB;
-      o[nt][3] *= alB;
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-    pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-    pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-    pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+        for (int e = 0; e < 4; ++e) {
+          const int key = key0 + 8 * nt + 2 * c + (e & 1);
+          const int lim = (e < 2) ? limA : limB;
+          sc[nt][e] = (key < lim) ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        }
 
-    // O (16 rows x 128 dims) += P V
+      float tA = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float tB = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
+      tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
+      tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
+      tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
+      const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+      const float uA = (nA == -INFINITY) ? 0.f : nA;
+      const float uB = (nB == -INFINITY) ? 0.f : nB;
+      const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
+      mA = nA;
+      mB = nB;
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      const int key = ((mat & 1) << 3) + mrow;
-      const int ch = 2 * dp + (mat >> 1);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_trans(vt + (ch >> 3) * kHalfTileBytes + swz128(key, ch & 7), v0, v1, v2, v3);
-      mma_bf16(o[2 * dp], pa, v0, v1);
-      mma_bf16(o[2 * dp + 1], pa, v2, v3);
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - uA);
+        sc[nt][1] = exp2f(sc[nt][1] - uA);
+        sc[nt][2] = exp2f(sc[nt][2] - uB);
+        sc[nt][3] = exp2f(sc[nt][3] - uB);
+      }
+      lA = lA * alA + (sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]);
+      lB = lB * alB + (sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]);
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] *= alA;
+        o[nt][1] *= alA;
+        o[nt][2] *= alB;
+        o[nt][3] *= alB;
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+
+      // O (16 rows x 128 dims) += P V
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        const int key = ((mat & 1) << 3) + mrow;
+        const int ch = 2 * dp + (mat >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vt + (ch >> 3) * kHalfTileBytes + swz128(key, ch & 7), v0, v1, v2, v3);
+        mma_bf16(o[2 * dp], pa, v0, v1);
+        mma_bf16(o[2 * dp + 1], pa, v2, v3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
 
-  lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-  lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
 
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int rr = half ? rB : rA;
-    if (rr >= R) continue;
-    const float l = half ? lB : lA;
-    const float m = half ? mB : mA;
-    const int t = rr / a.group, gi = rr - t * a.group;
-    const int64_t row = out_row(a, b, t, kvh * a.group + gi);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    if (a.num_splits == 1) {
-      __nv_bfloat16* orow = a.out + row * kHeadDim;
+    for (int half = 0; half < 2; ++half) {
+      const int rr = half ? rB : rA;
+      if (rr >= R) continue;
+      const float l = half ? lB : lA;
+      const float m = half ? mB : mA;
+      const int t = rr / a.group, gi = rr - t * a.group;
+      const RowDest d = row_dest<HPC>(a, seg, t, hh, gi);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (d.out != nullptr) {
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * c) =
-            pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
-      if (c == 0 && a.lse_out != nullptr) a.lse_out[row] = final_lse(m, l);
-    } else {
-      float* orow = a.ws_o + (row * a.num_splits + split) * kHeadDim;
+        for (int nt = 0; nt < 16; ++nt)
+          *reinterpret_cast<uint32_t*>(d.out + 8 * nt + 2 * c) =
+              pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (c == 0 && d.lse != nullptr) *d.lse = final_lse(m, l);
+      } else {
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<float2*>(orow + 8 * nt + 2 * c) =
-            make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
-      if (c == 0) a.ws_lse[row * a.num_splits + split] = final_lse(m, l);
+        for (int nt = 0; nt < 16; ++nt)
+          *reinterpret_cast<float2*>(d.po + 8 * nt + 2 * c) =
+              make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (c == 0) *d.plse = final_lse(m, l);
+      }
     }
   }
 }
@@ -501,9 +715,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   __shared__ uint64_t empty[STAGES];
   __shared__ int abort_flag;
   __shared__ int issued;
+  __shared__ Plan plan;
+  __shared__ long long wsum[32];
   uint8_t* stages = align1024(smem_raw);
 
-  const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -515,14 +730,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     fence_barrier_init();
   }
   __syncthreads();
+  // launched as a programmatic dependent: everything below may read what the
+  // previous kernel in the stream wrote (q, appended K/V, tables, lengths)
+  pdl_launch_dependents();
+  pdl_wait();
 
-  const SplitRange r = split_range(a, b, split);
+  if (a.num_splits == 0) {
+    make_plan(a, &plan, wsum);
+    write_empty_units(a, HPC);
+  }
   if (warp == HPC) {
-    produce<HPC, STAGES>(&kmap, &vmap, a, b, hg, r, stages, full, empty, &abort_flag, &issued);
+    produce<HPC, STAGES>(&kmap, &vmap, a, &plan, stages, full, empty, &abort_flag, &issued);
   } else if (TC) {
-    consume_tc<HPC, STAGES>(a, b, split, hg, r, stages, full, empty, &abort_flag);
+    consume_tc<HPC, STAGES>(a, &plan, stages, full, empty, &abort_flag);
   } else {
-    consume_simt<HPC, STAGES, R>(a, b, split, hg, r, stages, full, empty, &abort_flag);
+    consume_simt<HPC, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
   }
   __syncthreads();
   if (abort_flag && threadIdx.x == HPC * 32) drain<STAGES>(full, issued);
@@ -530,26 +752,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
 template <int HPC, int R, bool TC>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
-                       cudaStream_t stream) {
+                       int grid_ctas, cudaStream_t stream) {
   using Geo = Geometry<HPC>;
   auto kern = paged_decode_kernel<HPC, R, TC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Geo::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_splits, a.num_kv_heads / HPC, a.batch);
-  kern<<<grid, Geo::kThreads, Geo::kSmemBytes, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  const dim3 grid = a.num_splits == 0 ? dim3(grid_ctas, 1, 1)
+                                      : dim3(a.num_splits, a.num_kv_heads / HPC, a.batch);
+  return launch_pdl(kern, grid, dim3(Geo::kThreads), Geo::kSmemBytes, stream, kmap, vmap, a);
 }
 
 template <int HPC>
 cudaError_t launch_hpc(const DecodePlan& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const DecodeArgs& a, cudaStream_t stream) {
-  if (p.tensor_core) return launch_one<HPC, 16, true>(kmap, vmap, a, stream);
+                       const DecodeArgs& a, int grid_ctas, cudaStream_t stream) {
+  if (p.tensor_core) return launch_one<HPC, 16, true>(kmap, vmap, a, grid_ctas, stream);
   switch (p.rows) {
-    case 1: return launch_one<HPC, 1, false>(kmap, vmap, a, stream);
-    case 2: return launch_one<HPC, 2, false>(kmap, vmap, a, stream);
-    case 3: return launch_one<HPC, 3, false>(kmap, vmap, a, stream);
-    case 4: return launch_one<HPC, 4, false>(kmap, vmap, a, stream);
+    case 1: return launch_one<HPC, 1, false>(kmap, vmap, a, grid_ctas, stream);
+    case 2: return launch_one<HPC, 2, false>(kmap, vmap, a, grid_ctas, stream);
+    case 3: return launch_one<HPC, 3, false>(kmap, vmap, a, grid_ctas, stream);
+    case 4: return launch_one<HPC, 4, false>(kmap, vmap, a, grid_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -567,13 +789,13 @@ DecodePlan plan_decode(int num_kv_heads, int rows) {
 }
 
 cudaError_t launch_paged_decode(const DecodePlan& p, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, const DecodeArgs& a,
+                                const CUtensorMap& vmap, const DecodeArgs& a, int grid_ctas,
                                 cudaStream_t stream) {
   switch (p.heads_per_cta) {
-    case 8: return launch_hpc<8>(p, kmap, vmap, a, stream);
-    case 4: return launch_hpc<4>(p, kmap, vmap, a, stream);
-    case 2: return launch_hpc<2>(p, kmap, vmap, a, stream);
-    case 1: return launch_hpc<1>(p, kmap, vmap, a, stream);
+    case 8: return launch_hpc<8>(p, kmap, vmap, a, grid_ctas, stream);
+    case 4: return launch_hpc<4>(p, kmap, vmap, a, grid_ctas, stream);
+    case 2: return launch_hpc<2>(p, kmap, vmap, a, grid_ctas, stream);
+    case 1: return launch_hpc<1>(p, kmap, vmap, a, grid_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -42,12 +42,16 @@ struct DecodeArgs {
   int32_t batch, q_len, num_q_heads, num_kv_heads, group;
   int32_t block_size;
   int64_t num_blocks;
-  int32_t num_splits, chunk_pages;
+  int32_t num_splits;            // 0: balanced persistent schedule; >= 1: split schedule
+  int32_t chunk_pages;           // split schedule: pages per split
+  int32_t groups;                // kv-head groups (num_kv_heads / heads per CTA)
+  int32_t rows_per_unit;         // q_len * heads per CTA * group: rows of one (seq, group)
   float scale_log2;              // softmax scale * log2(e)
-  __nv_bfloat16* out;            // num_splits == 1: final bf16 output
-  float* lse_out;                // num_splits == 1: optional lse
-  float* ws_o;                   // num_splits > 1: partial outputs
-  float* ws_lse;                 // num_splits > 1: partial lse
+  __nv_bfloat16* out;            // final bf16 output
+  float* lse_out;                // optional final lse
+  float* ws_o;                   // partial outputs (split / balanced schedules)
+  float* ws_lse;                 // partial lse
+  int2* unit_info;               // balanced: first and last CTA of every (seq, group) unit
   int32_t* status_flags;
 };
 
@@ -60,11 +64,15 @@ struct DecodePlan {
 
 DecodePlan plan_decode(int num_kv_heads, int rows);
 
+// grid_ctas: CTAs of the balanced schedule (one per SM); unused otherwise.
 cudaError_t launch_paged_decode(const DecodePlan& plan, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, const DecodeArgs& a,
+                                const CUtensorMap& vmap, const DecodeArgs& a, int grid_ctas,
                                 cudaStream_t stream);
 
 cudaError_t launch_lse_combine(const float* ws_o, const float* ws_lse, int rows, int num_splits,
                                __nv_bfloat16* out, float* lse_out, cudaStream_t stream);
+
+// Merge of the balanced schedule's partials (units cut across CTAs only).
+cudaError_t launch_balanced_combine(const DecodeArgs& a, int heads_per_cta, cudaStream_t stream);
 
 }  // namespace pkvqk

@@ -71,6 +71,7 @@ def test_decode_validation_errors(lib):
     assert _decode(lib, lay, Hq=64, q_len=3) == lib.PKVQK_ERR_UNSUPPORTED   # 24 rows per kv head
     assert _decode(lib, lay, S=257) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, S=-1) == lib.PKVQK_ERR_INVALID_ARG
+    assert _decode(lib, lay, S=0, ws=100) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
     assert _decode(lib, lay, S=4, ws=100) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
     assert _decode(lib, lay, maxp=0) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, qs=(2048, 100)) == lib.PKVQK_ERR_INVALID_ARG   # q head stride % 8
@@ -115,6 +116,7 @@ def test_combine_validation_errors(lib):
 
 def test_workspace_bytes_formula(lib):
     assert lib.decode_workspace_bytes(4, 1, 16, 128, 1) == 0
+    assert lib.decode_workspace_bytes(4, 1, 16, 128, 0) > 0       # balanced schedule bound
     for B, T, Hq, S in [(4, 1, 16, 4), (64, 1, 16, 19), (32, 5, 16, 8), (1, 1, 8, 2)]:
         raw = B * T * Hq * S * 129 * 4
         assert lib.decode_workspace_bytes(B, T, Hq, 128, S) == (raw + 255) // 256 * 256

@@ -21,20 +21,22 @@ pytestmark = pytest.mark.gpu
 
 def _decode(lib, p, q=None, num_splits=1, hint=None, lse=True, k_cache=None, v_cache=None,
             flags=None, scale=0.0):
-    """Run pkvqk_paged_decode; num_splits=0 lets the library choose (the
-    workspace is sized with the same host-side heuristic call it documents)."""
+    """Run pkvqk_paged_decode; num_splits=0 is the balanced schedule, -1 uses
+    the library's split heuristic (pkvqk_choose_num_splits) explicitly."""
     q = p.q if q is None else q
     k_cache = p.k_cache if k_cache is None else k_cache
     v_cache = p.v_cache if v_cache is None else v_cache
     out = torch.full((p.B, p.q_len, p.Hq, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse_out = torch.full((p.B, p.q_len, p.Hq), float("nan"), device="cuda") if lse else None
     hint = p.max_seq_len if hint is None else hint
-    S = num_splits if num_splits > 0 else lib.choose_num_splits(
-        p.B, p.Hkv, p.q_len * p.Hq // p.Hkv, max(hint, 1), p.B * max(hint, 1), p.block_size)
+    S = num_splits
+    if S < 0:
+        S = lib.choose_num_splits(p.B, p.Hkv, p.q_len * p.Hq // p.Hkv, max(hint, 1),
+                                  p.total_tokens, p.block_size)
     nbytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
     lib.paged_decode(q, k_cache, v_cache, p.block_tables, p.seq_lens, out, q_len=p.q_len,
-                     num_splits=num_splits, max_seq_len_hint=hint, scale=scale, lse_out=lse_out,
+                     num_splits=S, max_seq_len_hint=hint, scale=scale, lse_out=lse_out,
                      workspace=ws, status_flags=flags)
     torch.cuda.synchronize()
     return out, lse_out, S
@@ -46,7 +48,7 @@ def _check(p, out, lse_out, seqs=None, what=""):
     return assert_attention_close(bits(out[sel]), ref, lse_out[sel].cpu().numpy(), ref_lse, what)
 
 
-@pytest.mark.parametrize("S", [1, 4])
+@pytest.mark.parametrize("S", [0, 1, 4, -1])
 def test_decode_tiny_all_rows(lib, S):
     p = workloads.decode_tiny(device="cuda")
     out, lse, _ = _decode(lib, p, num_splits=S)
@@ -82,7 +84,7 @@ def test_chained_norm_rope_append_then_decode(lib):
 @pytest.mark.parametrize("batch,ctx", [(1, 512), (8, 512), (8, 2048), (4, 8192)])
 def test_decode_uniform_small_points_all_rows(lib, batch, ctx):
     p = workloads.decode_uniform(batch, ctx, device="cuda")
-    for S in (1, 0):
+    for S in (1, 0, -1):
         out, lse, S_used = _decode(lib, p, num_splits=S)
         _check(p, out, lse, what=f"b{batch} ctx{ctx} S={S_used}")
 
@@ -97,7 +99,7 @@ def test_decode_uniform_64x8192_sampled(lib):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("S", [0, 1, 8, 32, 128])
+@pytest.mark.parametrize("S", [0, -1, 1, 8, 32, 128])
 def test_decode_long_32k_sampled(lib, S):
     p = workloads.decode_long(device="cuda")
     out, lse, S_used = _decode(lib, p, num_splits=S)
@@ -107,6 +109,8 @@ def test_decode_long_32k_sampled(lib, S):
 def test_gqa8_tensor_core_path_sampled(lib):
     p = workloads.decode_gqa8(device="cuda")
     out, lse, S = _decode(lib, p, num_splits=0)
+    _check(p, out, lse, seqs=[3, 40], what="gqa8 balanced")
+    out, lse, S = _decode(lib, p, num_splits=-1)
     order = np.argsort(p.seq_lens_host)
     seqs = sorted({int(order[0]), int(order[1]), int(order[32]), int(order[-1]), 7})
     _check(p, out, lse, seqs=seqs, what=f"gqa8 S={S}")
@@ -116,15 +120,16 @@ def test_gqa8_tensor_core_path_sampled(lib):
 def test_gqa8_small_all_rows(lib):
     p = workloads.make_problem("gqa8_small", 32, 4, 128, 16, [1, 17, 40, 300, 16, 33], 1, 64,
                                905, "cuda")
-    for S in (1, 3):
+    for S in (0, 1, 3):
         out, lse, _ = _decode(lib, p, num_splits=S)
         _check(p, out, lse, what=f"gqa8 small S={S}")
 
 
 def test_verify_causal_sampled(lib):
     p = workloads.verify_causal(device="cuda")
-    out, lse, S = _decode(lib, p, num_splits=0)
-    _check(p, out, lse, seqs=[0, 9, 31], what=f"verify S={S}")
+    for S in (0, -1):
+        out, lse, S_used = _decode(lib, p, num_splits=S)
+        _check(p, out, lse, seqs=[0, 9, 31], what=f"verify S={S_used}")
 
 
 @pytest.mark.parametrize("q_len,Hq,Hkv", [(5, 16, 8), (2, 16, 8), (3, 8, 8), (4, 32, 8), (2, 32, 4)])
@@ -132,7 +137,7 @@ def test_multi_query_small_all_rows(lib, q_len, Hq, Hkv):
     # rows per kv head = q_len * group covers both kernel families (<=4 and 5..16)
     lens = [q_len, q_len + 1, 16 + q_len, 100, 37]
     p = workloads.make_problem("mq", Hq, Hkv, 128, 16, lens, q_len, 40, 906 + q_len, "cuda")
-    for S in (1, 2):
+    for S in (0, 1, 2):
         out, lse, _ = _decode(lib, p, num_splits=S)
         _check(p, out, lse, what=f"q_len={q_len} Hq={Hq} Hkv={Hkv} S={S}")
 
@@ -144,7 +149,7 @@ def test_edge_lengths_and_empty_sequence(lib):
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     p.seq_lens = sl
     p.seq_lens_host = np.asarray(lens, np.int64)
-    for S in (1, 3):
+    for S in (0, 1, 3):
         out, lse, _ = _decode(lib, p, num_splits=S)
         assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
         _check(p, out, lse, seqs=list(range(1, len(lens))), what=f"edges S={S}")
@@ -155,17 +160,38 @@ def test_larger_block_sizes(lib, bs):
     lens = [1, bs - 1, bs, bs + 1, 3 * bs + 7]
     nb = sum(-(-n // bs) for n in lens) + 3
     p = workloads.make_problem(f"bs{bs}", 16, 8, 128, bs, lens, 1, nb, 908, "cuda")
-    for S in (1, 2):
+    for S in (0, 1, 2):
         out, lse, _ = _decode(lib, p, num_splits=S)
         _check(p, out, lse, what=f"bs={bs} S={S}")
+
+
+def test_balanced_schedule_mixed_lengths_all_rows(lib):
+    """One long sequence cut across many CTAs next to short ones, empties, and
+    more CTAs than pages elsewhere in the list."""
+    lens = [0, 3, 16, 17, 6000, 1, 0, 95, 2048, 33]
+    p = workloads.make_problem("mixed", 16, 8, 128, 16, [max(n, 1) for n in lens], 1,
+                               sum(-(-max(n, 1) // 16) for n in lens) + 4, 915, "cuda")
+    p.seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    p.seq_lens_host = np.asarray(lens, np.int64)
+    out, lse, _ = _decode(lib, p, num_splits=0)
+    for b in (0, 6):
+        assert torch.all(out[b] == 0) and torch.all(torch.isneginf(lse[b]))
+    _check(p, out, lse, seqs=[1, 2, 3, 4, 5, 7, 8, 9], what="balanced mixed")
+
+
+def test_balanced_schedule_tiny_batch_fewer_pages_than_ctas(lib):
+    p = workloads.make_problem("tiny1", 16, 8, 128, 16, [40], 1, 3, 916, "cuda")
+    out, lse, _ = _decode(lib, p, num_splits=0)
+    _check(p, out, lse, what="balanced 1 seq, 3 pages")
 
 
 def test_interleaved_cache_view_no_copy(lib):
     # K/V as strided views of a (num_blocks, 2, block_size, Hkv, D) allocation
     p = workloads.make_problem("kvstack", 16, 8, 128, 16, [40, 3, 77], 1, 16, 909, "cuda")
     both = torch.stack([p.k_cache, p.v_cache], dim=1).contiguous()
-    out, lse, _ = _decode(lib, p, num_splits=2, k_cache=both[:, 0], v_cache=both[:, 1])
-    _check(p, out, lse, what="interleaved cache")
+    for S in (0, 2):
+        out, lse, _ = _decode(lib, p, num_splits=S, k_cache=both[:, 0], v_cache=both[:, 1])
+        _check(p, out, lse, what=f"interleaved cache S={S}")
 
 
 def test_partials_plus_combine_equals_decode(lib):
@@ -225,10 +251,11 @@ def test_combine_standalone_against_oracle(lib):
     assert np.abs(g[fin] - ref_lse[fin]).max() < 1e-5
 
 
-def test_block_permutation_invariance_and_determinism(lib):
+@pytest.mark.parametrize("S", [0, 3])
+def test_block_permutation_invariance_and_determinism(lib, S):
     p = workloads.decode_uniform(4, 2048, device="cuda")
-    out1, lse1, _ = _decode(lib, p, num_splits=3)
-    out1b, lse1b, _ = _decode(lib, p, num_splits=3)
+    out1, lse1, _ = _decode(lib, p, num_splits=S)
+    out1b, lse1b, _ = _decode(lib, p, num_splits=S)
     assert torch.equal(out1, out1b) and torch.equal(lse1, lse1b)     # bit-identical reruns
     perm = torch.randperm(p.num_blocks, generator=torch.Generator().manual_seed(3)).cuda()
     kc2 = torch.empty_like(p.k_cache)
@@ -237,7 +264,7 @@ def test_block_permutation_invariance_and_determinism(lib):
     vc2[perm] = p.v_cache
     bt2 = perm[p.block_tables.long()].to(torch.int32)
     p2 = workloads.Problem(**{**p.__dict__, "block_tables": bt2})
-    out2, lse2, _ = _decode(lib, p2, num_splits=3, k_cache=kc2, v_cache=vc2)
+    out2, lse2, _ = _decode(lib, p2, num_splits=S, k_cache=kc2, v_cache=vc2)
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
 
 
@@ -246,15 +273,16 @@ def test_bad_block_id_is_flagged_not_faulted(lib):
     bt = p.block_tables.clone()
     bt[0, 1] = p.num_blocks + 100        # out of range: TMA fills zeros, flag raised
     p2 = workloads.Problem(**{**p.__dict__, "block_tables": bt})
-    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, lse, _ = _decode(lib, p2, num_splits=1, flags=flags)
-    assert flags.item() & lib.FLAG_BAD_BLOCK_ID
-    # the untouched sequence is still right
-    _check(p, out, lse, seqs=[1], what="bad block, other seq")
+    for S in (1, 0):
+        flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, lse, _ = _decode(lib, p2, num_splits=S, flags=flags)
+        assert flags.item() & lib.FLAG_BAD_BLOCK_ID
+        # the untouched sequence is still right
+        _check(p, out, lse, seqs=[1], what=f"bad block, other seq S={S}")
 
 
 def test_custom_scale(lib):
     p = workloads.decode_tiny(device="cuda")
-    out, lse, _ = _decode(lib, p, num_splits=2, scale=0.05)
+    out, lse, _ = _decode(lib, p, num_splits=0, scale=0.05)
     ref, ref_lse = oracle_attention(p, bits(p.q), scale=0.05)
     assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "scale 0.05")
