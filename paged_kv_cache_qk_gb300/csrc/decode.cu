@@ -15,7 +15,7 @@
 //     split takes the rest);
 //   * balanced (num_splits == 0): a persistent grid of one CTA per SM; the
 //     pages of all (head group, sequence) units are laid end to end and CTA c
-//     takes pages [c*TP/G, (c+1)*TP/G) of that list, crossing sequence
+//     takes pages [c*TP/G, (c+1)*TP/G) of that list (G = min(grid, TP)), crossing sequence
 //     boundaries without refilling its pipeline.  A unit that one CTA covers
 //     whole is written straight to the output; a unit cut across CTAs leaves
 //     one partial per CTA in slot (cta + unit), merged by the combine kernel.
@@ -90,6 +90,7 @@ __device__ __forceinline__ void set_range(Segment& s, int k0, int k1) {
 // Balanced schedule of this CTA: its page range and where its walk starts.
 struct Plan {
   long long tp, lo, hi;     // total pages; this CTA's pages [lo, hi)
+  long long g_eff;          // CTAs that get pages: min(grid, total pages)
   int u_start;              // first unit with pages at or after lo
   long long s_start;        // pages before unit u_start
 };
@@ -155,10 +156,9 @@ struct SegmentSource {
       seg.dest = whole ? kDestFinal : kDestSlot;
       seg.slot = static_cast<long long>(blockIdx.x) + cur;
       // the CTA holding the unit's first page records which CTAs cut it:
-      // page x belongs to CTA floor(((x + 1) * G - 1) / TP)
+      // page x belongs to CTA floor(((x + 1) * G' - 1) / TP), G' = g_eff
       if (start >= plan->lo && threadIdx.x == 0) {
-        const long long G = gridDim.x;
-        const int c_last = static_cast<int>((s * G - 1) / plan->tp);
+        const int c_last = static_cast<int>((s * plan->g_eff - 1) / plan->tp);
         a->unit_info[cur] = make_int2(blockIdx.x, c_last);
       }
       return true;
@@ -197,8 +197,11 @@ __device__ void make_plan(const DecodeArgs& a, Plan* plan, long long* wsum) {
   __syncthreads();
   const long long tp = wsum[nwarps - 1];
   const long long before = (warp ? wsum[warp - 1] : 0) + v - mine;   // pages before u_lo
-  const long long G = gridDim.x, c = blockIdx.x;
-  const long long lo = c * tp / G, hi = (c + 1) * tp / G;
+  // with fewer pages than CTAs only the first tp CTAs get pages, so that
+  // every CTA between a unit's first and last owner holds some of it
+  const long long G = min(static_cast<long long>(gridDim.x), tp > 0 ? tp : 1);
+  const long long c = blockIdx.x;
+  const long long lo = c < G ? c * tp / G : tp, hi = c < G ? (c + 1) * tp / G : tp;
   long long run = before;
   for (int u = u_lo; u < u_hi; ++u) {
     const long long P = unit_pages(a, u);
@@ -218,6 +221,7 @@ __device__ void make_plan(const DecodeArgs& a, Plan* plan, long long* wsum) {
     plan->tp = tp;
     plan->lo = lo;
     plan->hi = hi;
+    plan->g_eff = G;
     if (plan->u_start == U) plan->s_start = tp;
   }
   __syncthreads();
