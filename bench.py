@@ -232,7 +232,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkvqk", choices=["pkvqk", "reference"])
     ap.add_argument("--workload", default="decode_64x8192", choices=sorted(WORKLOADS))
-    ap.add_argument("--num-splits", type=int, default=0,
+    ap.add_argument("--num-splits", type=int, default=-1,
                     help="0: balanced persistent schedule; -1: split heuristic; >0: fixed splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

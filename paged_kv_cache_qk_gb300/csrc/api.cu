@@ -112,10 +112,10 @@ pkvqk_status get_encoder() {
 
 // 5-D view of a paged cache for the decode kernel's TMA boxes:
 //   dims (inner first) = (64 dims, slot, dim half, kv head, block),
-// box = (64, 16 slots, 2, heads_per_cta, 1 block), 128-byte swizzle, so the
-// shared-memory tile of one (kv head, half) is 16 slot rows of 128 bytes.
+// box = (64, tile_keys slots, 2, heads_per_cta, 1 block), 128-byte swizzle,
+// so the shared-memory tile of one (kv head, half) is tile_keys rows of 128 B.
 pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_cache_layout& L,
-                              int heads_per_cta) {
+                              int heads_per_cta, int tile_keys) {
   PKVQK_TRY(get_encoder());
   cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(L.block_size), 2,
                         static_cast<cuuint64_t>(L.num_kv_heads),
@@ -123,7 +123,8 @@ pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_ca
   cuuint64_t strides[4] = {static_cast<cuuint64_t>(L.slot_stride) * 2, 128,
                            static_cast<cuuint64_t>(L.head_stride) * 2,
                            static_cast<cuuint64_t>(L.block_stride) * 2};
-  cuuint32_t box[5] = {64, 16, 2, static_cast<cuuint32_t>(heads_per_cta), 1};
+  cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_keys), 2,
+                       static_cast<cuuint32_t>(heads_per_cta), 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -246,8 +247,8 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
 
   CUtensorMap kmap, vmap;
-  PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta));
-  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta));
+  PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta, plan.tile_keys));
+  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta, plan.tile_keys));
 
   const int hint_pages = (hint + L.block_size - 1) / L.block_size;
   pkvqk::DecodeArgs a;
@@ -393,8 +394,9 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
   const int64_t max_pages = (max_seq_len + block_size - 1) / block_size;
   const int64_t tot_pages =
       std::max<int64_t>((total_tokens + block_size - 1) / block_size, max_pages);
-  // Model: one resident CTA per SM; a wave of CTAs lasts as long as its
-  // longest split (chunk pages) plus a fixed start-up cost worth ~2 pages.
+  // Model: plan.ctas_per_sm resident CTAs per SM; a wave of CTAs lasts as
+  // long as its longest split (chunk pages) plus a fixed start-up cost worth
+  // ~2 pages.
   const double startup_pages = 2.0;
   double best_t = 1e300;
   int best = 1;
@@ -404,7 +406,8 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
     const int64_t splits_per_seq_avg =
         std::max<int64_t>(1, (tot_pages + batch * chunk - 1) / (batch * chunk));
     const int64_t ctas = groups * batch * std::min<int64_t>(splits_per_seq_avg, S);
-    const int64_t waves = (ctas + sm_count - 1) / sm_count;
+    const int64_t slots = static_cast<int64_t>(sm_count) * plan.ctas_per_sm;
+    const int64_t waves = (ctas + slots - 1) / slots;
     double t = static_cast<double>(waves) * (static_cast<double>(chunk) + startup_pages);
     if (S > 1) t += 0.5;                                             // combine launch
     if (t < best_t * 0.999) {

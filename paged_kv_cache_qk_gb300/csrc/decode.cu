@@ -46,10 +46,29 @@ namespace {
 
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int HPC>
+// Tile / ring choices per kv-head group size (measured on GB300; see the
+// notes in Config below).
+#ifndef PKVQK_HPC8_SIMT_TK
+#define PKVQK_HPC8_SIMT_TK 16
+#endif
+#ifndef PKVQK_HPC8_SIMT_BUDGET
+#define PKVQK_HPC8_SIMT_BUDGET 192
+#endif
+#ifndef PKVQK_HPC8_TC_BUDGET
+#define PKVQK_HPC8_TC_BUDGET 192
+#endif
+#ifndef PKVQK_HPC4_BUDGET
+#define PKVQK_HPC4_BUDGET 192
+#endif
+
+// HPC kv heads per CTA, TK keys per tile (one TMA box covers TK consecutive
+// slots of a page), stage ring of at most BUDGET_KB kilobytes.
+template <int HPC, int TK, int BUDGET_KB>
 struct Geometry {
+  static constexpr int kHalfTileBytes = TK * 128;       // (kv head, 64-dim half): TK rows x 128 B
+  static constexpr int kHeadTileBytes = 2 * kHalfTileBytes;
   static constexpr int kStageBytes = 2 * HPC * kHeadTileBytes;        // K + V tiles
-  static constexpr int kStagesRaw = (192 * 1024) / kStageBytes;
+  static constexpr int kStagesRaw = (BUDGET_KB * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;      // + alignment slack
   static constexpr int kThreads = (HPC + 1) * 32;
@@ -81,10 +100,10 @@ __device__ __forceinline__ long long unit_pages(const DecodeArgs& a, int u) {
   return (L + a.block_size - 1) / a.block_size;
 }
 
-__device__ __forceinline__ void set_range(Segment& s, int k0, int k1) {
+__device__ __forceinline__ void set_range(Segment& s, int k0, int k1, int tk) {
   s.k0 = k0;
   s.k1 = k1;
-  s.ntiles = k1 > k0 ? (k1 - k0 + kTileKeys - 1) / kTileKeys : 0;
+  s.ntiles = k1 > k0 ? (k1 - k0 + tk - 1) / tk : 0;
 }
 
 // Balanced schedule of this CTA: its page range and where its walk starts.
@@ -100,14 +119,16 @@ struct Plan {
 struct SegmentSource {
   const DecodeArgs* a;
   const Plan* plan;
+  int tk;                   // keys per tile
   int balanced;
   int done;
   int u;
   long long s;              // pages before unit u
 
-  __device__ void init(const DecodeArgs& args, const Plan* p) {
+  __device__ void init(const DecodeArgs& args, const Plan* p, int tile_keys) {
     a = &args;
     plan = p;
+    tk = tile_keys;
     balanced = args.num_splits == 0;
     done = 0;
     u = 0;
@@ -132,7 +153,7 @@ struct SegmentSource {
       int p1 = (seg.split == a->num_splits - 1) ? P : p0 + a->chunk_pages;
       p0 = min(p0, P);
       p1 = min(p1, P);
-      set_range(seg, p0 * a->block_size, min(p1 * a->block_size, seg.seq_len));
+      set_range(seg, p0 * a->block_size, min(p1 * a->block_size, seg.seq_len), tk);
       seg.dest = a->num_splits == 1 ? kDestFinal : kDestSplit;
       return true;
     }
@@ -151,7 +172,7 @@ struct SegmentSource {
       seg.split = 0;
       seg.seq_len = clamped_len(*a, seg.b);
       set_range(seg, static_cast<int>(plo) * a->block_size,
-                min(static_cast<int>(phi) * a->block_size, seg.seq_len));
+                min(static_cast<int>(phi) * a->block_size, seg.seq_len), tk);
       const bool whole = plo == 0 && phi == P;
       seg.dest = whole ? kDestFinal : kDestSlot;
       seg.slot = static_cast<long long>(blockIdx.x) + cur;
@@ -255,11 +276,12 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 // ----------------------------------------------------------------- producer
 
-template <int HPC, int STAGES>
+template <int HPC, int TK, int BUDGET, int STAGES>
 __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& a,
                         const Plan* plan, uint8_t* stages, uint64_t* full, uint64_t* empty,
                         volatile int* abort_flag, int* issued_out) {
-  constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
+  using Geo = Geometry<HPC, TK, BUDGET>;
+  constexpr int kStageBytes = Geo::kStageBytes;
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
     prefetch_tensormap(kmap);
@@ -267,7 +289,7 @@ __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const 
   }
   const uint64_t pol = l2_evict_first_policy();
   SegmentSource src;
-  src.init(a, plan);
+  src.init(a, plan, TK);
   Segment seg;
   int it = 0;                      // tiles issued so far (ring position)
   bool ok = true;
@@ -277,7 +299,7 @@ __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const 
       int blk = 0, slot0 = 0;
       const int i = i0 + lane;
       if (i < seg.ntiles) {
-        const int key = seg.k0 + i * kTileKeys;
+        const int key = seg.k0 + i * TK;
         const int page = key / a.block_size;
         slot0 = key - page * a.block_size;
         blk = __ldg(bt + page);
@@ -296,8 +318,8 @@ __device__ void produce(const CUtensorMap* kmap, const CUtensorMap* vmap, const 
             uint8_t* dst = stages + s * kStageBytes;
             // coordinates: (dim lo, slot, dim half, kv head, block)
             tma_load_5d(dst, kmap, &full[s], 0, sj, 0, seg.hg * HPC, bj, pol);
-            tma_load_5d(dst + HPC * kHeadTileBytes, vmap, &full[s], 0, sj, 0, seg.hg * HPC, bj,
-                        pol);
+            tma_load_5d(dst + HPC * Geo::kHeadTileBytes, vmap, &full[s], 0, sj, 0, seg.hg * HPC,
+                        bj, pol);
           } else {
             *abort_flag = 1;
             report(a.status_flags, kFlagTimeout);
@@ -360,17 +382,21 @@ __device__ __forceinline__ float final_lse(float m, float l) {
 
 // ------------------------------------------------------ CUDA-core consumer
 
-template <int HPC, int STAGES, int R>
+template <int HPC, int TK, int BUDGET, int STAGES, int R>
 __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_t* stages,
                              uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
-  constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
+  using Geo = Geometry<HPC, TK, BUDGET>;
+  constexpr int kStageBytes = Geo::kStageBytes;
+  constexpr int kHalfTileBytes = Geo::kHalfTileBytes;
+  constexpr int kHeadTileBytes = Geo::kHeadTileBytes;
+  constexpr int kQuads = TK / 4;   // 4 keys per warp step
   const int lane = threadIdx.x & 31;
   const int hh = threadIdx.x >> 5;
   const int kg = lane >> 3;        // key group: key 4*q4 + kg of the tile
   const int p = lane & 7;          // 16-byte chunk p of each 64-dim half
 
   SegmentSource src;
-  src.init(a, plan);
+  src.init(a, plan, TK);
   Segment seg;
   int it = 0;                      // tiles consumed so far (ring position)
   bool aborted = false;
@@ -408,11 +434,11 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
       }
       const uint8_t* kt = stages + s * kStageBytes + hh * kHeadTileBytes;
       const uint8_t* vt = kt + HPC * kHeadTileBytes;
-      const int key0 = seg.k0 + i * kTileKeys;
+      const int key0 = seg.k0 + i * TK;
 
-      float sc[R][4];
+      float sc[R][kQuads];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kQuads; ++q4) {
         const int row = q4 * 4 + kg;
         const uint4 k0 = *reinterpret_cast<const uint4*>(kt + swz128(row, p));
         const uint4 k1 = *reinterpret_cast<const uint4*>(kt + kHalfTileBytes + swz128(row, p));
@@ -432,17 +458,19 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
         }
       }
 
-      float pr[R][4];
+      float pr[R][kQuads];
 #pragma unroll
       for (int rr = 0; rr < R; ++rr) {
-        const float mt = fmaxf(fmaxf(sc[rr][0], sc[rr][1]), fmaxf(sc[rr][2], sc[rr][3]));
+        float mt = sc[rr][0];
+#pragma unroll
+        for (int q4 = 1; q4 < kQuads; ++q4) mt = fmaxf(mt, sc[rr][q4]);
         const float mn = fmaxf(m[rr], mt);
         const float mu = (mn == -INFINITY) ? 0.f : mn;
         const float alpha = exp2f(m[rr] - mu);
         m[rr] = mn;
         float ls = l[rr] * alpha;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < kQuads; ++q4) {
           pr[rr][q4] = exp2f(sc[rr][q4] - mu);
           ls += pr[rr][q4];
         }
@@ -452,7 +480,7 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
       }
 
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kQuads; ++q4) {
         const int row = q4 * 4 + kg;
         const uint4 v0 = *reinterpret_cast<const uint4*>(vt + swz128(row, p));
         const uint4 v1 = *reinterpret_cast<const uint4*>(vt + kHalfTileBytes + swz128(row, p));
@@ -549,10 +577,14 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int HPC, int STAGES>
+template <int HPC, int TK, int BUDGET, int STAGES>
 __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t* stages,
                            uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
-  constexpr int kStageBytes = Geometry<HPC>::kStageBytes;
+  static_assert(TK == 16, "the mma tiles take 16 keys per tile");
+  using Geo = Geometry<HPC, TK, BUDGET>;
+  constexpr int kStageBytes = Geo::kStageBytes;
+  constexpr int kHalfTileBytes = Geo::kHalfTileBytes;
+  constexpr int kHeadTileBytes = Geo::kHeadTileBytes;
   const int lane = threadIdx.x & 31;
   const int hh = threadIdx.x >> 5;
   const int g = lane >> 2;         // fragment row group
@@ -564,7 +596,7 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
   const int mrow = lane & 7;
 
   SegmentSource src;
-  src.init(a, plan);
+  src.init(a, plan, TK);
   Segment seg;
   int it = 0;                      // tiles consumed so far (ring position)
   bool aborted = false;
@@ -605,7 +637,7 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
       }
       const uint32_t kt = smem_addr(stages + s * kStageBytes + hh * kHeadTileBytes);
       const uint32_t vt = kt + HPC * kHeadTileBytes;
-      const int key0 = seg.k0 + i * kTileKeys;
+      const int key0 = seg.k0 + i * TK;
 
       // S (16 rows x 16 keys) = Q K^T
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -709,11 +741,11 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
 
 // ------------------------------------------------------------------ kernel
 
-template <int HPC, int R, bool TC>
-__global__ void __launch_bounds__(Geometry<HPC>::kThreads, 1)
+template <int HPC, int TK, int BUDGET, int R, bool TC>
+__global__ void __launch_bounds__(Geometry<HPC, TK, BUDGET>::kThreads, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  constexpr int STAGES = Geometry<HPC>::kStages;
+  constexpr int STAGES = Geometry<HPC, TK, BUDGET>::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[STAGES];
   __shared__ uint64_t empty[STAGES];
@@ -744,21 +776,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     write_empty_units(a, HPC);
   }
   if (warp == HPC) {
-    produce<HPC, STAGES>(&kmap, &vmap, a, &plan, stages, full, empty, &abort_flag, &issued);
+    produce<HPC, TK, BUDGET, STAGES>(&kmap, &vmap, a, &plan, stages, full, empty, &abort_flag,
+                                     &issued);
   } else if (TC) {
-    consume_tc<HPC, STAGES>(a, &plan, stages, full, empty, &abort_flag);
+    consume_tc<HPC, TK, BUDGET, STAGES>(a, &plan, stages, full, empty, &abort_flag);
   } else {
-    consume_simt<HPC, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
+    consume_simt<HPC, TK, BUDGET, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
   }
   __syncthreads();
   if (abort_flag && threadIdx.x == HPC * 32) drain<STAGES>(full, issued);
 }
 
-template <int HPC, int R, bool TC>
+template <int HPC, int TK, int BUDGET, int R, bool TC>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
                        int grid_ctas, cudaStream_t stream) {
-  using Geo = Geometry<HPC>;
-  auto kern = paged_decode_kernel<HPC, R, TC>;
+  using Geo = Geometry<HPC, TK, BUDGET>;
+  auto kern = paged_decode_kernel<HPC, TK, BUDGET, R, TC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Geo::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -767,17 +800,58 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
   return launch_pdl(kern, grid, dim3(Geo::kThreads), Geo::kSmemBytes, stream, kmap, vmap, a);
 }
 
+// Per head count: the CUDA-core path's tile and ring, and the mma path's.
+template <int HPC>
+struct Config;
+template <>
+struct Config<8> {
+  static constexpr int kSimtTK = PKVQK_HPC8_SIMT_TK, kSimtBudget = PKVQK_HPC8_SIMT_BUDGET;
+  static constexpr int kTcBudget = PKVQK_HPC8_TC_BUDGET;
+};
+template <>
+struct Config<4> {
+  static constexpr int kSimtTK = 16, kSimtBudget = PKVQK_HPC4_BUDGET;
+  static constexpr int kTcBudget = PKVQK_HPC4_BUDGET;
+};
+template <>
+struct Config<2> {
+  static constexpr int kSimtTK = 16, kSimtBudget = 96;
+  static constexpr int kTcBudget = 96;
+};
+template <>
+struct Config<1> {
+  static constexpr int kSimtTK = 16, kSimtBudget = 64;
+  static constexpr int kTcBudget = 64;
+};
+
 template <int HPC>
 cudaError_t launch_hpc(const DecodePlan& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const DecodeArgs& a, int grid_ctas, cudaStream_t stream) {
-  if (p.tensor_core) return launch_one<HPC, 16, true>(kmap, vmap, a, grid_ctas, stream);
+  using C = Config<HPC>;
+  if (p.tensor_core)
+    return launch_one<HPC, 16, C::kTcBudget, 16, true>(kmap, vmap, a, grid_ctas, stream);
+  constexpr int TK = C::kSimtTK, B = C::kSimtBudget;
   switch (p.rows) {
-    case 1: return launch_one<HPC, 1, false>(kmap, vmap, a, grid_ctas, stream);
-    case 2: return launch_one<HPC, 2, false>(kmap, vmap, a, grid_ctas, stream);
-    case 3: return launch_one<HPC, 3, false>(kmap, vmap, a, grid_ctas, stream);
-    case 4: return launch_one<HPC, 4, false>(kmap, vmap, a, grid_ctas, stream);
+    case 1: return launch_one<HPC, TK, B, 1, false>(kmap, vmap, a, grid_ctas, stream);
+    case 2: return launch_one<HPC, TK, B, 2, false>(kmap, vmap, a, grid_ctas, stream);
+    case 3: return launch_one<HPC, TK, B, 3, false>(kmap, vmap, a, grid_ctas, stream);
+    case 4: return launch_one<HPC, TK, B, 4, false>(kmap, vmap, a, grid_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int HPC>
+void fill_plan(DecodePlan& p) {
+  using C = Config<HPC>;
+  const int tk = p.tensor_core ? 16 : C::kSimtTK;
+  const int budget = p.tensor_core ? C::kTcBudget : C::kSimtBudget;
+  p.tile_keys = tk;
+  const int stage = 2 * HPC * 2 * tk * 128;
+  int stages = budget * 1024 / stage;
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  const int smem = stages * stage + 1024 + 512;       // + static shared memory
+  p.ctas_per_sm = smem > 0 ? (228 * 1024) / smem : 1;
+  if (p.ctas_per_sm < 1) p.ctas_per_sm = 1;
 }
 
 }  // namespace
@@ -789,6 +863,12 @@ DecodePlan plan_decode(int num_kv_heads, int rows) {
   p.heads_per_cta = hpc;
   p.tensor_core = rows > 4;
   p.rows = rows;
+  switch (hpc) {
+    case 8: fill_plan<8>(p); break;
+    case 4: fill_plan<4>(p); break;
+    case 2: fill_plan<2>(p); break;
+    default: fill_plan<1>(p); break;
+  }
   return p;
 }
 

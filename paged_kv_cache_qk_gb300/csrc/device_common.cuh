@@ -32,12 +32,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Keys per pipeline tile: one TMA box covers 16 consecutive slots of a page.
-constexpr int kTileKeys = 16;
 constexpr int kHeadDim = 128;
-// bytes of one (kv head, 64-element half) sub-tile: 16 rows x 128 B, 128B swizzle
-constexpr int kHalfTileBytes = kTileKeys * 128;
-constexpr int kHeadTileBytes = 2 * kHalfTileBytes;            // both halves of D
 
 // ~2^31 cycles (about 1 s at the 2 GHz clock) before a pipeline wait gives up.
 constexpr long long kWaitLimitCycles = 1ll << 31;
