@@ -778,10 +778,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (warp == HPC) {
     produce<HPC, TK, BUDGET, STAGES>(&kmap, &vmap, a, &plan, stages, full, empty, &abort_flag,
                                      &issued);
-  } else if (TC) {
-    consume_tc<HPC, TK, BUDGET, STAGES>(a, &plan, stages, full, empty, &abort_flag);
   } else {
-    consume_simt<HPC, TK, BUDGET, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
+    if constexpr (TC)
+      consume_tc<HPC, TK, BUDGET, STAGES>(a, &plan, stages, full, empty, &abort_flag);
+    else
+      consume_simt<HPC, TK, BUDGET, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
   }
   __syncthreads();
   if (abort_flag && threadIdx.x == HPC * 32) drain<STAGES>(full, issued);
