@@ -133,11 +133,12 @@ PKVQK_API pkvqk_status pkvqk_norm_rope_append(
     int32_t* status_flags, pkvqk_stream_t stream);
 
 /*
- * Split count for pkvqk_paged_decode from host-side facts only (no device
+ * Schedule for pkvqk_paged_decode from host-side facts only (no device
  * read): batch, kv heads, rows per kv head (q_len * Hq/Hkv), the longest
  * sequence, the total key count and the SM count (0 = query the current
- * device).  Returns a value in [1, 256].  Source: the "decode routing hint
- * (host side, zero device sync)" of InfiniLM PR #585, Summary item 3.
+ * device).  Returns 0 (the balanced schedule: chosen for large batches of
+ * mixed lengths) or a split count in [1, 256].  Source: the "decode routing
+ * hint (host side, zero device sync)" of InfiniLM PR #585, Summary item 3.
  */
 PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
                                 int32_t rows_per_kv_head, int32_t max_seq_len,

@@ -127,9 +127,14 @@ def test_split_heuristic_is_host_only_and_bounded(lib):
     for B, hkv, rows, L, sms in [(1, 8, 2, 512, 148), (64, 8, 2, 8192, 152), (8, 8, 2, 32768, 152),
                                  (64, 4, 8, 16384, 152), (32, 8, 10, 8197, 152), (4, 8, 2, 1, 152)]:
         S = lib.choose_num_splits(B, hkv, rows, L, B * L, 16, sms)
-        assert 1 <= S <= 256
+        assert 1 <= S <= 256                      # uniform lengths: a split count
         assert S <= max(1, -(-L // 16))           # never more splits than pages
     # a single long sequence is spread over many splits; a full batch is not split much
     assert lib.choose_num_splits(8, 8, 2, 32768, 8 * 32768, 16, 152) >= 8
     assert lib.choose_num_splits(1, 8, 2, 512, 512, 16, 152) >= 2
     assert lib.choose_num_splits(0, 8, 2, 512, 0, 16, 152) == 1
+    # large batch of mixed lengths: the balanced schedule
+    assert lib.choose_num_splits(64, 4, 8, 16384, 230000, 16, 152) == 0
+    assert lib.choose_num_splits(32, 8, 10, 8197, 172000, 16, 152) == 0
+    # small mixed batch: still a split count
+    assert lib.choose_num_splits(4, 8, 2, 256, 600, 16, 152) >= 1
