@@ -5,7 +5,7 @@
 // every decision comes from host arguments (InfiniLM PR #585, "概述 /
 // Summary" item 3: decode routing decided on the host with zero device sync),
 // so every entry point can be recorded into a CUDA graph.
-#include "../../include/pkvqk.h"
+#include "pkvqk.h"
 #include "kernels.h"
 
 #include <cudaTypedefs.h>

@@ -14,7 +14,7 @@
 // (it names a host-side shadow), so its device address is looked up once per
 // device with cudaGetSymbolAddress, with that device current, on the first
 // call made on that device.
-#include "../../include/pkvqk.h"
+#include "pkvqk.h"
 
 #include <cuda_runtime.h>
 
