@@ -60,40 +60,24 @@ constexpr float kLn2 = 0.693147180559945309f;
 #ifndef PKVQK_HPC4_BUDGET
 #define PKVQK_HPC4_BUDGET 192
 #endif
-#ifndef PKVQK_TC_WPH
-#define PKVQK_TC_WPH 1
-#endif
 #ifndef PKVQK_TC_ILP
 #define PKVQK_TC_ILP 0
 #endif
 
 // HPC kv heads per CTA, TK keys per tile (one TMA box covers TK consecutive
 // slots of a page), stage ring of at most BUDGET_KB kilobytes.
-// WPH consumer warps per kv head (mma path: they take alternate tiles and
-// merge through shared memory at the end of a segment).
-template <int HPC, int TK, int BUDGET_KB, int WPH = 1>
+template <int HPC, int TK, int BUDGET_KB>
 struct Geometry {
   static constexpr int kHalfTileBytes = TK * 128;       // (kv head, 64-dim half): TK rows x 128 B
   static constexpr int kHeadTileBytes = 2 * kHalfTileBytes;
   static constexpr int kStageBytes = 2 * HPC * kHeadTileBytes;        // K + V tiles
   static constexpr int kStagesRaw = (BUDGET_KB * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-  static constexpr int kXchgBytes = WPH > 1 ? HPC * 32 * 68 * 4 : 0;  // pair-merge scratch
-  static constexpr int kSmemBytes = kStages * kStageBytes + kXchgBytes + 1024;
-  static constexpr int kConsumers = HPC * WPH;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;      // + alignment slack
+  static constexpr int kConsumers = HPC;
   static constexpr int kThreads = (kConsumers + 1) * 32;
 };
 
-// Consumer warps per kv head for a kernel variant: the mma path may use two
-// (at most 4 heads per CTA, so 9 warps keep ~160 registers without spills).
-template <int HPC, bool TC>
-constexpr int warps_per_head() {
-  return (TC && HPC <= 4) ? PKVQK_TC_WPH : 1;
-}
-
-__device__ __forceinline__ void pair_barrier(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
 
 constexpr int kDestFinal = 0;   // bf16 output + lse
 constexpr int kDestSplit = 1;   // partial at [row][split] (split schedule)
@@ -598,18 +582,16 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int HPC, int TK, int BUDGET, int STAGES, int WPH>
+template <int HPC, int TK, int BUDGET, int STAGES>
 __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t* stages,
-                           float* xchg, uint64_t* full, uint64_t* empty,
-                           volatile int* abort_flag) {
+                           uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   static_assert(TK == 16, "the mma tiles take 16 keys per tile");
-  using Geo = Geometry<HPC, TK, BUDGET, WPH>;
+  using Geo = Geometry<HPC, TK, BUDGET>;
   constexpr int kStageBytes = Geo::kStageBytes;
   constexpr int kHalfTileBytes = Geo::kHalfTileBytes;
   constexpr int kHeadTileBytes = Geo::kHeadTileBytes;
   const int lane = threadIdx.x & 31;
-  const int hh = (threadIdx.x >> 5) / WPH;   // kv head within the CTA
-  const int sub = (threadIdx.x >> 5) % WPH;  // this warp takes tiles i with i % WPH == sub
+  const int hh = threadIdx.x >> 5;           // kv head within the CTA
   const int g = lane >> 2;         // fragment row group
   const int c = lane & 3;          // thread in group
   const int R = a.q_len * a.group;
@@ -651,7 +633,6 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
     for (int i = 0; i < seg.ntiles; ++i, ++it) {
-      if (WPH > 1 && (i % WPH) != sub) continue;
       const int s = it % STAGES;
       if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
         *abort_flag = 1;
@@ -746,42 +727,6 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    if (WPH > 1) {
-      // the second warp of the pair hands its state to the first
-      float* x = xchg + (hh * 32 + lane) * 68;
-      if (sub == 1) {
-        x[0] = mA;
-        x[1] = mB;
-        x[2] = lA;
-        x[3] = lB;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-          *reinterpret_cast<float4*>(x + 4 + 4 * nt) =
-              make_float4(o[nt][0], o[nt][1], o[nt][2], o[nt][3]);
-      }
-      pair_barrier(1 + hh);
-      if (sub == 0) {
-        const float mA2 = x[0], mB2 = x[1], lA2 = x[2], lB2 = x[3];
-        const float nA = fmaxf(mA, mA2), nB = fmaxf(mB, mB2);
-        const float uA = (nA == -INFINITY) ? 0.f : nA, uB = (nB == -INFINITY) ? 0.f : nB;
-        const float a1 = exp2f(mA - uA), a2 = exp2f(mA2 - uA);
-        const float b1 = exp2f(mB - uB), b2 = exp2f(mB2 - uB);
-        lA = lA * a1 + lA2 * a2;
-        lB = lB * b1 + lB2 * b2;
-        mA = nA;
-        mB = nB;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          const float4 v = *reinterpret_cast<const float4*>(x + 4 + 4 * nt);
-          o[nt][0] = o[nt][0] * a1 + v.x * a2;
-          o[nt][1] = o[nt][1] * a1 + v.y * a2;
-          o[nt][2] = o[nt][2] * b1 + v.z * b2;
-          o[nt][3] = o[nt][3] * b1 + v.w * b2;
-        }
-      }
-      pair_barrier(1 + hh);           // the slot is free again
-      if (sub == 1) continue;
-    }
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -817,11 +762,10 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
 // ------------------------------------------------------------------ kernel
 
 template <int HPC, int TK, int BUDGET, int R, bool TC>
-__global__ void __launch_bounds__(Geometry<HPC, TK, BUDGET, warps_per_head<HPC, TC>()>::kThreads, 1)
+__global__ void __launch_bounds__(Geometry<HPC, TK, BUDGET>::kThreads, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  constexpr int WPH = warps_per_head<HPC, TC>();
-  using Geo = Geometry<HPC, TK, BUDGET, WPH>;
+  using Geo = Geometry<HPC, TK, BUDGET>;
   constexpr int STAGES = Geo::kStages;
   constexpr int kProducer = Geo::kConsumers;    // warp index of the producer
   extern __shared__ uint8_t smem_raw[];
@@ -858,8 +802,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                      &issued);
   } else {
     if constexpr (TC) {
-      float* xchg = reinterpret_cast<float*>(stages + STAGES * Geo::kStageBytes);
-      consume_tc<HPC, TK, BUDGET, STAGES, WPH>(a, &plan, stages, xchg, full, empty, &abort_flag);
+      consume_tc<HPC, TK, BUDGET, STAGES>(a, &plan, stages, full, empty, &abort_flag);
     } else {
       consume_simt<HPC, TK, BUDGET, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
     }
@@ -871,7 +814,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 template <int HPC, int TK, int BUDGET, int R, bool TC>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
                        int grid_ctas, cudaStream_t stream) {
-  using Geo = Geometry<HPC, TK, BUDGET, warps_per_head<HPC, TC>()>;
+  using Geo = Geometry<HPC, TK, BUDGET>;
   auto kern = paged_decode_kernel<HPC, TK, BUDGET, R, TC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Geo::kSmemBytes);
@@ -930,8 +873,7 @@ void fill_plan(DecodePlan& p) {
   const int stage = 2 * HPC * 2 * tk * 128;
   int stages = budget * 1024 / stage;
   stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  const int xchg = (p.tensor_core && HPC <= 4 && PKVQK_TC_WPH > 1) ? HPC * 32 * 68 * 4 : 0;
-  const int smem = stages * stage + xchg + 1024 + 512;       // + static shared memory
+  const int smem = stages * stage + 1024 + 512;       // + static shared memory
   p.ctas_per_sm = smem > 0 ? (228 * 1024) / smem : 1;
   if (p.ctas_per_sm < 1) p.ctas_per_sm = 1;
 }
