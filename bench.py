@@ -57,6 +57,26 @@ for _b in (1, 8, 32, 64):
                              f"Qwen3-0.6B decode 16q/8kv D128 bf16 bs16, batch {_b} x ctx {_c}"))
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode-kernel launch,
+# mean of two launches from the 1-pass ncu capture recorded in
+# profiles/paged_decode_kernel_decode_64x8192.md.  A capture describes the
+# kernel sources it was taken with: when the sources hash differently, the
+# bench reports traffic as null.
+MEASURED_TRAFFIC = {
+    "decode_64x8192": {"src": "d83bf47c18b4e7c0", "bytes": 2149753472, "num_splits": 2},
+}
+
+
+def kernel_src_hash():
+    import hashlib
+    csrc = os.path.join(ROOT, "paged_kv_cache_qk_gb300", "csrc")
+    parts = []
+    for f in ("decode.cu", "device_common.cuh", "kernels.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            parts.append(hashlib.sha256(fh.read()).hexdigest())
+    return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -376,6 +396,9 @@ def main():
     e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
 
     peak, peak_kind = load_peaks()
+    rec = MEASURED_TRAFFIC.get(args.workload)
+    traffic = (rec["bytes"] if rec and rec["src"] == kernel_src_hash() and rec["num_splits"] == S
+               else None)
     dec_avg_ms = statistics.fmean(decode_ms)
     achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
 
@@ -417,7 +440,7 @@ def main():
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None,
+            "traffic": traffic,
             "algorithmic_bytes_per_launch": decode_bytes,
             "avg_launch_ms": round(dec_avg_ms, 5),
         },
