@@ -148,9 +148,11 @@ PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
 /*
  * Workspace bytes pkvqk_paged_decode needs on the current device:
  * - num_splits == 1: 0;
- * - num_splits >= 2: batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up to
- *   256.  Layout: fp32 partial outputs [rows][num_splits][head_dim] followed
- *   by fp32 partial lse [rows][num_splits], rows = (b*q_len + t)*Hq + h;
+ * - num_splits >= 2: (batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up
+ *   to 16) + batch*Hq*4, rounded up to 256.  Layout: fp32 partial outputs
+ *   [rows][num_splits][head_dim], fp32 partial lse [rows][num_splits]
+ *   (rows = (b*q_len + t)*Hq + h), then int32 per-(sequence, kv-head group)
+ *   arrival counters;
  * - num_splits == 0 (balanced): an upper bound for any kv-head count,
  *   ((SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded up, where
  *   SMs is the current device's multiprocessor count (internal layout).
@@ -176,9 +178,10 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   block_size) / num_splits) pages, split j < S-1 of a sequence covers pages
  *   [j*C, (j+1)*C) and split S-1 covers [(S-1)*C, end), so every key is
  *   covered whatever the hint.  Each split keeps an online softmax; for
- *   num_splits > 1 the partials go to the workspace and the LSE combine
- *   (launched by this call) merges them.  pkvqk_choose_num_splits gives a
- *   host-side choice of S.
+ *   num_splits > 1 the partials go to the workspace and the CTA that
+ *   finishes a sequence's last split merges them by log-sum-exp inside the
+ *   same kernel (it counts arrivals; no CTA waits for another).
+ *   pkvqk_choose_num_splits gives a host-side choice.
  * - num_splits == 0 (balanced): one CTA per SM; the pages of all (sequence,
  *   kv-head group) pairs are laid end to end and every CTA takes an equal
  *   contiguous share, crossing sequence boundaries; a sequence covered by one
@@ -195,7 +198,10 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   lse_out       device fp32 [batch, q_len, Hq] or NULL
  *   workspace     device, >= pkvqk_decode_workspace_bytes(batch, q_len, Hq,
  *                 head_dim, num_splits) on the current device (NULL if 0);
- *                 contents need no initialisation
+ *                 zero-filled before its first use (e.g. cudaMemsetAsync);
+ *                 every call leaves it reusable without clearing (its
+ *                 counters return to zero), unless a call reports
+ *                 PKVQK_FLAG_WAIT_TIMEOUT
  * Supported: head_dim 128, Hq % Hkv == 0, q_len*Hq/Hkv <= 16.
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode(
@@ -211,8 +217,8 @@ PKVQK_API pkvqk_status pkvqk_paged_decode(
 
 /*
  * As pkvqk_paged_decode but stops after the split pass: the partials stay in
- * the workspace (layout above) and no combine is launched.  num_splits must
- * be >= 2 (no heuristic).
+ * the workspace (layout above) and are not merged (pkvqk_lse_combine merges
+ * them).  num_splits must be >= 2 (no heuristic).
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode_partials(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,

@@ -159,9 +159,11 @@ size_t balanced_bytes(int64_t slot_rows, int64_t units) {
   return (raw + 255) & ~size_t(255);
 }
 
-// Bytes of the fp32 partials [rows][S][128] + partial lse [rows][S].
-size_t partial_bytes(int64_t rows, int S) {
-  const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
+// Split schedule: fp32 partials [rows][S][128] + partial lse [rows][S], then
+// int32 arrival counters [units] (units <= batch x Hq).
+size_t partial_bytes(int64_t rows, int S, int64_t units) {
+  const size_t raw = align16(static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float)) +
+                     static_cast<size_t>(units) * 4;
   return (raw + 255) & ~size_t(255);
 }
 
@@ -221,7 +223,7 @@ pkvqk_status run_decode(const DecodeCall& c) {
   const int64_t slot_rows = (grid_ctas + units) * rows_per_unit;
   size_t need = 0;
   if (S == 0) need = balanced_bytes(slot_rows, units);
-  else if (c.partials_only || S > 1) need = partial_bytes(nrows, S);
+  else if (c.partials_only || S > 1) need = partial_bytes(nrows, S, units);
   if (need > 0 && c.workspace_bytes < need)
     return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
                 c.workspace_bytes, need);
@@ -276,6 +278,7 @@ pkvqk_status run_decode(const DecodeCall& c) {
   a.ws_o = nullptr;
   a.ws_lse = nullptr;
   a.unit_info = nullptr;
+  a.unit_counter = nullptr;
   if (S == 0) {
     a.ws_o = static_cast<float*>(c.workspace);
     a.ws_lse = a.ws_o + slot_rows * 128;
@@ -284,7 +287,10 @@ pkvqk_status run_decode(const DecodeCall& c) {
   } else if (need > 0) {
     a.ws_o = static_cast<float*>(c.workspace);
     a.ws_lse = a.ws_o + nrows * S * 128;
+    a.unit_counter = reinterpret_cast<int32_t*>(
+        static_cast<char*>(c.workspace) + align16(static_cast<size_t>(nrows) * S * 129 * 4));
   }
+  a.fuse_combine = (S > 1 && !c.partials_only) ? 1 : 0;
   a.status_flags = c.status_flags;
 
   cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, grid_ctas, c.stream);
@@ -292,10 +298,6 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (S == 0) {
     e = pkvqk::launch_balanced_combine(a, plan.heads_per_cta, c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
-  } else if (S > 1 && !c.partials_only) {
-    e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
-                                  c.stream);
-    if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
   }
   return ok();
 }
@@ -430,7 +432,8 @@ size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_q_
     return balanced_bytes((sm_count_current() + static_cast<int64_t>(batch)) * per,
                           static_cast<int64_t>(batch) * num_q_heads);
   }
-  return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits);
+  return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits,
+                       static_cast<int64_t>(batch) * num_q_heads);
 }
 
 pkvqk_status pkvqk_paged_decode(const void* q, int64_t q_stride_t, int64_t q_stride_h,

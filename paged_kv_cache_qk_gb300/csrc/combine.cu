@@ -12,6 +12,7 @@
 // by shuffle.  Launched as a programmatic dependent of the decode kernel, so
 // its launch overlaps the decode tail; it waits for the partials before
 // reading them.
+#include "combine_row.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -20,62 +21,6 @@ namespace pkvqk {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr float kLog2e = 1.4426950408889634f;
-
-// Merge of n partial rows at ws index base + j * stride (j < n) into one
-// bf16 output row (+ lse); one warp.
-__device__ __forceinline__ void combine_row(const float* __restrict__ ws_o,
-                                            const float* __restrict__ ws_lse, long long base,
-                                            long long stride, int n, __nv_bfloat16* out_row,
-                                            float* lse_dst, int lane) {
-  // pass 1: the row's max lse (lane j holds split j, j + 32, ...)
-  float M = -INFINITY;
-  for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldg(ws_lse + base + j * stride));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-  // pass 2: weights in the lanes that own the splits, partial rows summed
-  // with 8 independent float4 loads in flight per lane
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int j0 = 0; j0 < n; j0 += 32) {
-      const int jl = j0 + lane;
-      const float lj = jl < n ? __ldg(ws_lse + base + jl * stride) : -INFINITY;
-      const float wl = (lj == -INFINITY) ? 0.f : exp2f((lj - M) * kLog2e);
-      wsum += wl;
-      const int cnt = min(32, n - j0);
-      for (int jj = 0; jj < cnt; jj += 8) {
-        float4 v[8];
-        float w[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          w[u] = __shfl_sync(0xffffffffu, wl, (jj + u) & 31);
-          const long long idx = base + static_cast<long long>(j0 + jj + u) * stride;
-          v[u] = (jj + u < cnt)
-                     ? __ldg(reinterpret_cast<const float4*>(ws_o + idx * kHeadDim + 4 * lane))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float ww = (jj + u < cnt) ? w[u] : 0.f;
-          acc.x = fmaf(ww, v[u].x, acc.x);
-          acc.y = fmaf(ww, v[u].y, acc.y);
-          acc.z = fmaf(ww, v[u].z, acc.z);
-          acc.w = fmaf(ww, v[u].w, acc.w);
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out_row + 4 * lane) = packed;
-  if (lane == 0 && lse_dst != nullptr) *lse_dst = wsum > 0.f ? M + logf(wsum) : -INFINITY;
-}
 
 __global__ void __launch_bounds__(kWarps * 32)
 lse_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int rows,
@@ -85,7 +30,7 @@ lse_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
-  combine_row(ws_o, ws_lse, row * S, 1, S, out + row * kHeadDim,
+  combine_row<false>(ws_o, ws_lse, row * S, 1, S, out + row * kHeadDim,
               lse_out != nullptr ? lse_out + row : nullptr, lane);
 }
 
@@ -110,7 +55,7 @@ balanced_combine_kernel(const DecodeArgs a, int hpc) {
   if (info.x == info.y) return;                 // written whole by one CTA
   const long long srow = (t * hpc + hh) * a.group + gi;
   const long long base = (static_cast<long long>(info.x) + u) * a.rows_per_unit + srow;
-  combine_row(a.ws_o, a.ws_lse, base, a.rows_per_unit, info.y - info.x + 1,
+  combine_row<false>(a.ws_o, a.ws_lse, base, a.rows_per_unit, info.y - info.x + 1,
               a.out + row * kHeadDim, a.lse_out != nullptr ? a.lse_out + row : nullptr, lane);
 }
 

@@ -34,7 +34,7 @@ def _decode(lib, p, q=None, num_splits=1, hint=None, lse=True, k_cache=None, v_c
         S = lib.choose_num_splits(p.B, p.Hkv, p.q_len * p.Hq // p.Hkv, max(hint, 1),
                                   p.total_tokens, p.block_size)
     nbytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
     lib.paged_decode(q, k_cache, v_cache, p.block_tables, p.seq_lens, out, q_len=p.q_len,
                      num_splits=S, max_seq_len_hint=hint, scale=scale, lse_out=lse_out,
                      workspace=ws, status_flags=flags)
@@ -199,7 +199,7 @@ def test_partials_plus_combine_equals_decode(lib):
     S = 5
     out, lse, _ = _decode(lib, p, num_splits=S)
     nbytes = lib.decode_workspace_bytes(p.B, 1, p.Hq, p.D, S)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     lib.paged_decode_partials(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, ws,
                               num_splits=S, max_seq_len_hint=p.max_seq_len)
     rows = p.B * p.Hq
@@ -223,6 +223,24 @@ def test_partials_plus_combine_equals_decode(lib):
     fin = np.isfinite(ref_l[:, 0])
     assert np.array_equal(np.isfinite(got_l), fin)
     assert np.abs(got_l[fin] - ref_l[:, 0][fin]).max() < 1e-3
+
+
+def test_workspace_reuse_keeps_counters_consistent(lib):
+    """One workspace, zeroed once, reused by calls with different split
+    counts: the in-kernel merge's counters return to zero after every call."""
+    p = workloads.decode_uniform(8, 2048, device="cuda")
+    nbytes = max(lib.decode_workspace_bytes(p.B, 1, p.Hq, p.D, S) for S in (3, 5, 8))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    ref, ref_lse = oracle_attention(p, bits(p.q), seqs=[2, 7])
+    for S in (3, 5, 3, 8, 5, 3):
+        out = torch.full((p.B, 1, p.Hq, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((p.B, 1, p.Hq), float("nan"), device="cuda")
+        lib.paged_decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                         num_splits=S, max_seq_len_hint=p.max_seq_len, lse_out=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all()
+        assert_attention_close(bits(out[[2, 7]]), ref, lse[[2, 7]].cpu().numpy(), ref_lse,
+                               f"reused workspace S={S}")
 
 
 def _compact(p, seqs):

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def test_step_captures_and_replays_bit_identically(lib, S):
     p = workloads.decode_uniform(8, 2048, device="cuda")
     nbytes = lib.decode_workspace_bytes(p.B, 1, p.Hq, p.D, S)
-    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda") if nbytes else None
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda") if nbytes else None
     q0 = p.q.clone()
     kc0, vc0 = p.k_cache.clone(), p.v_cache.clone()
 

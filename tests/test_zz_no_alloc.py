@@ -33,7 +33,7 @@ def _run_both(lib, p, S):
     out_ref = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
     lse_ref = torch.empty(shape[:3], device="cuda")
     ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
     lib.check(lib.pkvqk_paged_decode(
         _ptr(p.q), p.q.stride(0), p.q.stride(1), _ptr(p.k_cache), _ptr(p.v_cache),
         ctypes.byref(lay), _ptr(p.block_tables), p.block_tables.shape[1], _ptr(p.seq_lens),
