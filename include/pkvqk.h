@@ -148,11 +148,11 @@ PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
 /*
  * Workspace bytes pkvqk_paged_decode needs on the current device:
  * - num_splits == 1: 0;
- * - num_splits >= 2: (batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up
- *   to 16) + batch*Hq*4, rounded up to 256.  Layout: fp32 partial outputs
- *   [rows][num_splits][head_dim], fp32 partial lse [rows][num_splits]
- *   (rows = (b*q_len + t)*Hq + h), then int32 per-(sequence, kv-head group)
- *   arrival counters;
+ * - num_splits >= 2: 65536 + batch*q_len*Hq*num_splits*(head_dim + 1)*4,
+ *   rounded up to 256.  Layout: a 64 KiB region of int32 per-(sequence,
+ *   kv-head group) arrival counters, then fp32 partial outputs
+ *   [rows][num_splits][head_dim], then fp32 partial lse [rows][num_splits]
+ *   (rows = (b*q_len + t)*Hq + h);
  * - num_splits == 0 (balanced): an upper bound for any kv-head count,
  *   ((SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded up, where
  *   SMs is the current device's multiprocessor count (internal layout).

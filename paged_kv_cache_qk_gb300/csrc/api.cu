@@ -159,11 +159,14 @@ size_t balanced_bytes(int64_t slot_rows, int64_t units) {
   return (raw + 255) & ~size_t(255);
 }
 
-// Split schedule: fp32 partials [rows][S][128] + partial lse [rows][S], then
-// int32 arrival counters [units] (units <= batch x Hq).
-size_t partial_bytes(int64_t rows, int S, int64_t units) {
-  const size_t raw = align16(static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float)) +
-                     static_cast<size_t>(units) * 4;
+// Split schedule: a fixed region of int32 arrival counters (one per unit,
+// never used for anything else, so calls of any shape can share one
+// workspace), then fp32 partials [rows][S][128] and partial lse [rows][S].
+constexpr size_t kCounterBytes = 64 << 10;
+constexpr int64_t kMaxCounterUnits = kCounterBytes / 4;
+
+size_t partial_bytes(int64_t rows, int S) {
+  const size_t raw = kCounterBytes + static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
   return (raw + 255) & ~size_t(255);
 }
 
@@ -223,7 +226,7 @@ pkvqk_status run_decode(const DecodeCall& c) {
   const int64_t slot_rows = (grid_ctas + units) * rows_per_unit;
   size_t need = 0;
   if (S == 0) need = balanced_bytes(slot_rows, units);
-  else if (c.partials_only || S > 1) need = partial_bytes(nrows, S, units);
+  else if (c.partials_only || S > 1) need = partial_bytes(nrows, S);
   if (need > 0 && c.workspace_bytes < need)
     return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
                 c.workspace_bytes, need);
@@ -285,12 +288,13 @@ pkvqk_status run_decode(const DecodeCall& c) {
     a.unit_info = reinterpret_cast<int2*>(static_cast<char*>(c.workspace) +
                                           align16(static_cast<size_t>(slot_rows) * 129 * 4));
   } else if (need > 0) {
-    a.ws_o = static_cast<float*>(c.workspace);
+    a.unit_counter = static_cast<int32_t*>(c.workspace);
+    a.ws_o = reinterpret_cast<float*>(static_cast<char*>(c.workspace) + kCounterBytes);
     a.ws_lse = a.ws_o + nrows * S * 128;
-    a.unit_counter = reinterpret_cast<int32_t*>(
-        static_cast<char*>(c.workspace) + align16(static_cast<size_t>(nrows) * S * 129 * 4));
   }
-  a.fuse_combine = (S > 1 && !c.partials_only) ? 1 : 0;
+  // merge in the decode kernel unless the caller wants the partials, or the
+  // units outnumber the counter region (then a separate combine kernel runs)
+  a.fuse_combine = (S > 1 && !c.partials_only && units <= kMaxCounterUnits) ? 1 : 0;
   a.status_flags = c.status_flags;
 
   cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, grid_ctas, c.stream);
@@ -298,6 +302,10 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (S == 0) {
     e = pkvqk::launch_balanced_combine(a, plan.heads_per_cta, c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
+  } else if (S > 1 && !c.partials_only && !a.fuse_combine) {
+    e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
+                                  c.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
   }
   return ok();
 }
@@ -432,8 +440,7 @@ size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_q_
     return balanced_bytes((sm_count_current() + static_cast<int64_t>(batch)) * per,
                           static_cast<int64_t>(batch) * num_q_heads);
   }
-  return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits,
-                       static_cast<int64_t>(batch) * num_q_heads);
+  return partial_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits);
 }
 
 pkvqk_status pkvqk_paged_decode(const void* q, int64_t q_stride_t, int64_t q_stride_h,
