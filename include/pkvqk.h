@@ -14,6 +14,9 @@
  *      the causal multi-query verify of item 4 (k + 1 tokens per sequence).
  *   3. pkvqk_lse_combine      — item 1 ("splitkv"): log-sum-exp merge of the
  *      split partials.
+ *   4. pkvqk_paged_prefill    — item 4 (chunked prefill): the same causal
+ *      attention for many new tokens per sequence (a prefill chunk after
+ *      its prior context), on the tensor cores.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -281,6 +284,67 @@ PKVQK_API pkvqk_status pkvqk_lse_combine(const float* ws_o, const float* ws_lse,
                                int32_t rows, int32_t head_dim,
                                int32_t num_splits, void* out, float* lse_out,
                                pkvqk_stream_t stream);
+
+/*
+ * Split count for pkvqk_paged_prefill from host-side facts only: batch, kv
+ * heads, q_len, group (Hq/Hkv), the longest sequence (keys, counting the new
+ * tokens) and the SM count (0 = the current device's).  Returns 1..256: 1
+ * when the row tiles alone fill the GPU, else enough splits of >= 256 keys
+ * to give about one CTA per SM.
+ */
+PKVQK_API int32_t pkvqk_choose_prefill_splits(int32_t batch, int32_t num_kv_heads,
+                                    int32_t q_len, int32_t group,
+                                    int32_t max_seq_len, int32_t sm_count);
+
+/*
+ * Workspace bytes of pkvqk_paged_prefill: 0 for num_splits == 1, else
+ * batch*q_len*Hq*num_splits*(head_dim + 1)*4 rounded up to 256: fp32 partial
+ * outputs [rows][num_splits][head_dim] then fp32 partial lse
+ * [rows][num_splits], rows = (b*q_len + t)*Hq + h (the layout
+ * pkvqk_lse_combine reads).  Nothing in it needs to start at zero.
+ */
+PKVQK_API size_t pkvqk_prefill_workspace_bytes(int32_t batch, int32_t q_len,
+                                     int32_t num_q_heads, int32_t head_dim,
+                                     int32_t num_splits);
+
+/*
+ * Causal multi-query paged attention on the tensor cores: a chunked-prefill
+ * step (q_len new tokens per sequence, appended to the cache beforehand,
+ * attend to their prior context and causally to each other) or, with small
+ * q_len, a speculative-verify step.  Source: InfiniLM PR #585, "概述 /
+ * Summary" item 4 (chunked prefill; fixed b x (k+1) verify shape) and item 1
+ * (paged cache read through the block table).
+ *
+ * Same definition as pkvqk_paged_decode: query token t of sequence b sees the
+ * keys n < seq_lens[b] - q_len + t + 1; q head h reads kv head h / (Hq/Hkv);
+ * scale <= 0 selects head_dim^-1/2; a row with no visible key outputs 0 and
+ * lse = -inf.  The rows (t, h) of one kv head are packed t*group + h%group
+ * into tiles of 128, so one CTA's tile covers 128/group tokens.
+ *
+ * num_splits >= 1: split j covers pages [j*C, (j+1)*C) of every sequence,
+ * C = ceil(ceil(max_seq_len_hint / block_size) / num_splits), the last split
+ * also everything past (S-1)*C pages.  With num_splits > 1 the normalised
+ * partials go to the workspace and this call then launches the log-sum-exp
+ * combine (pkvqk_lse_combine) on the same stream.
+ *
+ *   q, out, lse_out, block_tables, seq_lens: as pkvqk_paged_decode
+ *   num_splits    1..256 (pkvqk_choose_prefill_splits gives a choice)
+ *   max_seq_len_hint  host int >= the longest seq_len (0 = max_blocks_per_seq*block_size)
+ *   workspace     device, >= pkvqk_prefill_workspace_bytes(...) (NULL if 0)
+ * Supported: head_dim 128, Hq % Hkv == 0, 1 <= q_len <= 16384,
+ * q_len*Hq/Hkv <= 65536.  One CTA per SM (192 KiB of shared memory and 512
+ * tensor-memory columns each).
+ */
+PKVQK_API pkvqk_status pkvqk_paged_prefill(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k_cache, const void* v_cache, const pkvqk_cache_layout* layout,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens,
+    int32_t batch, int32_t q_len, int32_t num_q_heads,
+    int32_t num_splits, int32_t max_seq_len_hint, float scale,
+    void* out, float* lse_out,
+    void* workspace, size_t workspace_bytes,
+    int32_t* status_flags, pkvqk_stream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -2,7 +2,8 @@
 
 Argument marshalling only: the ``pkvqk_*`` functions below have the C names
 and C arguments (integers for pointers, ints, floats); the short-named
-helpers (``norm_rope_append``, ``paged_decode``, ``lse_combine``) take torch
+helpers (``norm_rope_append``, ``paged_decode``, ``paged_prefill``,
+``lse_combine``) take torch
 tensors, read their data pointers and strides and call the C entry point on
 the current CUDA stream.  All computation happens in the library's kernels;
 if ``libpkvqk.so`` is missing or fails to load, importing this module raises.
@@ -93,12 +94,19 @@ pkvqk_lse_combine = _sig("pkvqk_lse_combine", ctypes.c_int,
 pkvqk_paged_decode_static_ws = _sig("pkvqk_paged_decode_static_ws", ctypes.c_int,
                                     _decode_args + [c_vp, c_vp, c_vp, c_vp])
 pkvqk_static_workspace_capacity = _sig("pkvqk_static_workspace_capacity", c_size, [])
+pkvqk_choose_prefill_splits = _sig("pkvqk_choose_prefill_splits", c_i32,
+                                   [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32])
+pkvqk_prefill_workspace_bytes = _sig("pkvqk_prefill_workspace_bytes", c_size,
+                                     [c_i32, c_i32, c_i32, c_i32, c_i32])
+pkvqk_paged_prefill = _sig("pkvqk_paged_prefill", ctypes.c_int,
+                           _decode_args + [c_vp, c_vp, c_vp, c_size, c_vp, c_vp])
 
 EXPORTED = [
     "pkvqk_last_error", "pkvqk_abi_version", "pkvqk_norm_rope_append",
     "pkvqk_choose_num_splits", "pkvqk_decode_workspace_bytes", "pkvqk_paged_decode",
     "pkvqk_paged_decode_partials", "pkvqk_lse_combine", "pkvqk_paged_decode_static_ws",
-    "pkvqk_static_workspace_capacity",
+    "pkvqk_static_workspace_capacity", "pkvqk_choose_prefill_splits",
+    "pkvqk_prefill_workspace_bytes", "pkvqk_paged_prefill",
 ]
 
 
@@ -207,3 +215,36 @@ def paged_decode_partials(q, k_cache, v_cache, block_tables, seq_lens, workspace
 def lse_combine(ws_o, ws_lse, rows, num_splits, out, lse_out=None, stream=None):
     check(pkvqk_lse_combine(_ptr(ws_o), _ptr(ws_lse), int(rows), 128, int(num_splits),
                             _ptr(out), _ptr(lse_out), _stream(stream)))
+
+
+def choose_prefill_splits(batch, num_kv_heads, q_len, group, max_seq_len, sm_count=0):
+    return int(pkvqk_choose_prefill_splits(batch, num_kv_heads, q_len, group, max_seq_len,
+                                           sm_count))
+
+
+def prefill_workspace_bytes(batch, q_len, num_q_heads, head_dim, num_splits):
+    return int(pkvqk_prefill_workspace_bytes(batch, q_len, num_q_heads, head_dim, num_splits))
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, out, *, q_len, num_splits=1,
+                  max_seq_len_hint=0, scale=0.0, lse_out=None, workspace=None,
+                  status_flags=None, stream=None):
+    """Causal multi-query attention on the tensor cores.
+
+    q [B*q_len, Hq, D]; out [B, q_len, Hq, D] (or [B*q_len, Hq, D]) contiguous bf16.
+    """
+    Tq, Hq, D = q.shape
+    B = Tq // q_len
+    lay = cache_layout(k_cache)
+    if tuple(v_cache.stride()) != tuple(k_cache.stride()) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must share one layout")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(pkvqk_paged_prefill(
+        _ptr(q), q.stride(0), q.stride(1),
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(lay),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        B, q_len, Hq, int(num_splits), int(max_seq_len_hint), float(scale),
+        _ptr(out), _ptr(lse_out), _ptr(workspace), ws_bytes,
+        _ptr(status_flags), _stream(stream)))

@@ -7,6 +7,7 @@
 // so every entry point can be recorded into a CUDA graph.
 #include "pkvqk.h"
 #include "kernels.h"
+#include "prefill.h"
 
 #include <cudaTypedefs.h>
 
@@ -110,12 +111,14 @@ pkvqk_status get_encoder() {
   return PKVQK_OK;
 }
 
-// 5-D view of a paged cache for the decode kernel's TMA boxes:
+// 5-D view of a paged cache for the kernels' TMA boxes:
 //   dims (inner first) = (64 dims, slot, dim half, kv head, block),
-// box = (64, tile_keys slots, 2, heads_per_cta, 1 block), 128-byte swizzle,
-// so the shared-memory tile of one (kv head, half) is tile_keys rows of 128 B.
+// box = (64, tile_keys slots, halves, heads_per_cta, 1 block), 128-byte
+// swizzle, so the shared-memory tile of one (kv head, half) is tile_keys rows
+// of 128 B.  The decode kernel takes both halves per box, the prefill kernel
+// one (it places the halves of all pages of a key tile in two blocks).
 pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_cache_layout& L,
-                              int heads_per_cta, int tile_keys) {
+                              int heads_per_cta, int tile_keys, int halves = 2) {
   PKVQK_TRY(get_encoder());
   cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(L.block_size), 2,
                         static_cast<cuuint64_t>(L.num_kv_heads),
@@ -123,7 +126,7 @@ pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_ca
   cuuint64_t strides[4] = {static_cast<cuuint64_t>(L.slot_stride) * 2, 128,
                            static_cast<cuuint64_t>(L.head_stride) * 2,
                            static_cast<cuuint64_t>(L.block_stride) * 2};
-  cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_keys), 2,
+  cuuint32_t box[5] = {64, static_cast<cuuint32_t>(tile_keys), static_cast<cuuint32_t>(halves),
                        static_cast<cuuint32_t>(heads_per_cta), 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
@@ -303,6 +306,111 @@ pkvqk_status run_decode(const DecodeCall& c) {
     e = pkvqk::launch_balanced_combine(a, plan.heads_per_cta, c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
   } else if (S > 1 && !c.partials_only && !a.fuse_combine) {
+    e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
+                                  c.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
+  }
+  return ok();
+}
+
+// --------------------------------------------------------------- prefill
+
+size_t prefill_bytes(int64_t rows, int S) {
+  if (S <= 1) return 0;
+  const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
+  return (raw + 255) & ~size_t(255);
+}
+
+pkvqk_status run_prefill(const DecodeCall& c) {
+  PKVQK_TRY(check_layout(c.layout));
+  const pkvqk_cache_layout& L = *c.layout;
+  if (c.batch < 0 || c.batch > 65535) return fail(PKVQK_ERR_INVALID_ARG, "batch %d", c.batch);
+  if (c.q_len < 1 || c.q_len > 16384)
+    return fail(PKVQK_ERR_INVALID_ARG, "q_len %d (1..16384)", c.q_len);
+  if (c.num_q_heads < 1 || (c.num_q_heads % L.num_kv_heads) != 0)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                c.num_q_heads, L.num_kv_heads);
+  const int group = c.num_q_heads / L.num_kv_heads;
+  const int64_t rows = static_cast<int64_t>(c.q_len) * group;
+  if (rows > 65536)
+    return fail(PKVQK_ERR_UNSUPPORTED, "q_len * group = %lld rows per kv head (max 65536)",
+                static_cast<long long>(rows));
+  if (c.max_blocks_per_seq < 1) return fail(PKVQK_ERR_INVALID_ARG, "max_blocks_per_seq < 1");
+  const int64_t cap_tokens = static_cast<int64_t>(c.max_blocks_per_seq) * L.block_size;
+  if (cap_tokens > INT32_MAX)
+    return fail(PKVQK_ERR_INVALID_ARG, "max_blocks_per_seq * block_size exceeds 2^31 - 1");
+  if (c.max_seq_len_hint < 0) return fail(PKVQK_ERR_INVALID_ARG, "max_seq_len_hint < 0");
+  if (c.num_splits < 1 || c.num_splits > 256)
+    return fail(PKVQK_ERR_INVALID_ARG, "num_splits %d (1..256)", c.num_splits);
+  if (c.q_stride_t % 8 || c.q_stride_h % 8 || c.q_stride_h < 1 || c.q_stride_t < 0)
+    return fail(PKVQK_ERR_INVALID_ARG, "q strides must be multiples of 8 elements");
+  if (!std::isfinite(c.scale)) return fail(PKVQK_ERR_INVALID_ARG, "scale is not finite");
+  const int S = c.num_splits;
+  const int m_tiles = static_cast<int>((rows + 127) / 128);
+  const int64_t grid_x = static_cast<int64_t>(m_tiles) * L.num_kv_heads * S;
+  if (grid_x > INT32_MAX) return fail(PKVQK_ERR_UNSUPPORTED, "too many CTAs (%lld)",
+                                      static_cast<long long>(grid_x));
+  const int64_t nrows = static_cast<int64_t>(c.batch) * c.q_len * c.num_q_heads;
+  const size_t need = prefill_bytes(nrows, S);
+  if (need > 0 && c.workspace_bytes < need)
+    return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
+                c.workspace_bytes, need);
+  if (c.batch == 0) return ok();
+
+  PKVQK_TRY(check_device_ptr(c.q, "q"));
+  PKVQK_TRY(check_device_ptr(c.k_cache, "k_cache"));
+  PKVQK_TRY(check_device_ptr(c.v_cache, "v_cache"));
+  PKVQK_TRY(check_device_ptr(c.block_tables, "block_tables"));
+  PKVQK_TRY(check_device_ptr(c.seq_lens, "seq_lens"));
+  PKVQK_TRY(check_device_ptr(c.out, "out"));
+  if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
+  if (!aligned16(c.q) || !aligned16(c.out))
+    return fail(PKVQK_ERR_INVALID_ARG, "q/out not 16-byte aligned");
+  if (!aligned16(c.k_cache) || !aligned16(c.v_cache))
+    return fail(PKVQK_ERR_INVALID_ARG, "cache base not 16-byte aligned");
+  if (need > 0) {
+    PKVQK_TRY(check_device_ptr(c.workspace, "workspace"));
+    if (!aligned16(c.workspace)) return fail(PKVQK_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  }
+  if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
+
+  // largest power of two dividing the page size, at most 128 (the kernel's
+  // key tile): no box crosses a page
+  const int box_slots = std::min(L.block_size & -L.block_size, 128);
+  CUtensorMap kmap, vmap;
+  PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, 1, box_slots, 1));
+  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, 1, box_slots, 1));
+
+  const int hint = c.max_seq_len_hint > 0 ? c.max_seq_len_hint : static_cast<int>(cap_tokens);
+  const int hint_pages = (hint + L.block_size - 1) / L.block_size;
+  pkvqk::PrefillArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(c.q);
+  a.q_stride_t = c.q_stride_t;
+  a.q_stride_h = c.q_stride_h;
+  a.block_tables = c.block_tables;
+  a.max_blocks_per_seq = c.max_blocks_per_seq;
+  a.seq_lens = c.seq_lens;
+  a.batch = c.batch;
+  a.q_len = c.q_len;
+  a.num_q_heads = c.num_q_heads;
+  a.num_kv_heads = L.num_kv_heads;
+  a.group = group;
+  a.block_size = L.block_size;
+  a.num_blocks = L.num_blocks;
+  a.num_splits = S;
+  a.chunk_pages = std::max(1, (hint_pages + S - 1) / S);
+  a.m_tiles = m_tiles;
+  const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(128.0f);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = static_cast<__nv_bfloat16*>(c.out);
+  a.lse_out = c.lse_out;
+  a.ws_o = S > 1 ? static_cast<float*>(c.workspace) : nullptr;
+  a.ws_lse = S > 1 ? a.ws_o + nrows * S * 128 : nullptr;
+  a.status_flags = c.status_flags;
+
+  cudaError_t e = pkvqk::launch_paged_prefill(kmap, vmap, a, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  if (S > 1) {
     e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
                                   c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
@@ -496,6 +604,42 @@ pkvqk_status pkvqk_lse_combine(const float* ws_o, const float* ws_lse, int32_t r
                                             reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
   return ok();
+}
+
+int32_t pkvqk_choose_prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t q_len,
+                                    int32_t group, int32_t max_seq_len, int32_t sm_count) {
+  if (batch <= 0 || num_kv_heads <= 0 || q_len <= 0 || group <= 0 || max_seq_len <= 0) return 1;
+  if (sm_count <= 0) sm_count = sm_count_current();
+  const int64_t m_tiles = (static_cast<int64_t>(q_len) * group + 127) / 128;
+  const int64_t ctas = static_cast<int64_t>(batch) * num_kv_heads * m_tiles;
+  if (ctas >= sm_count) return 1;
+  int64_t S = (sm_count + ctas - 1) / ctas;
+  S = std::min<int64_t>(S, std::max<int64_t>(1, max_seq_len / 256));
+  return static_cast<int32_t>(std::min<int64_t>(S, 256));
+}
+
+size_t pkvqk_prefill_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                     int32_t head_dim, int32_t num_splits) {
+  if (batch <= 0 || q_len <= 0 || num_q_heads <= 0 || head_dim != 128 || num_splits <= 1)
+    return 0;
+  return prefill_bytes(static_cast<int64_t>(batch) * q_len * num_q_heads, num_splits);
+}
+
+pkvqk_status pkvqk_paged_prefill(const void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                 const void* k_cache, const void* v_cache,
+                                 const pkvqk_cache_layout* layout, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                 int32_t num_splits, int32_t max_seq_len_hint, float scale,
+                                 void* out, float* lse_out, void* workspace,
+                                 size_t workspace_bytes_, int32_t* status_flags,
+                                 pkvqk_stream_t stream) {
+  DecodeCall c{q,          q_stride_t,  q_stride_h,       k_cache,    v_cache,
+               layout,     block_tables, max_blocks_per_seq, seq_lens, batch,
+               q_len,      num_q_heads, num_splits,       max_seq_len_hint, scale,
+               out,        lse_out,     workspace,        workspace_bytes_, status_flags,
+               reinterpret_cast<cudaStream_t>(stream), false};
+  return run_prefill(c);
 }
 
 }  // extern "C"

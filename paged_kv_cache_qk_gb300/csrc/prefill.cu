@@ -1,0 +1,534 @@
+// Causal multi-query attention over the paged K/V cache -- the chunked-prefill
+// step (many new tokens of one sequence at once) and, as its small case, the
+// speculative-verify step -- on the 5th-generation tensor cores (tcgen05,
+// accumulators in tensor memory, operands staged by TMA).
+//
+// Operation: InfiniLM PR #585 "perf: Qwen3 offline inference — hybrid
+// attention backend, fused rms_norm_rope, chunked prefill + prompt-lookup spec
+// decoding", section "概述 / Summary", items 1 and 4: new token t of sequence
+// b (t < q_len) sits at position seq_len - q_len + t and attends to the keys
+// n <= seq_len - q_len + t of its own sequence, gathered page by page through
+// the block table; q head h reads kv head h / group; softmax scale D^-1/2
+// unless the caller gives one.
+//
+// One CTA = one tile of 128 packed rows r = t * group + (h % group) of one
+// (sequence, kv head), restricted to one split of the key range.  Keys stream
+// in tiles of 128 through a two-stage ring (K and V released separately).
+// Warp roles:
+//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r).  Reads its
+//              score row S = Q K^T from tensor memory, keeps the running max
+//              and sum, writes P (bf16) to shared memory, rescales O in tensor
+//              memory only when the max grew by more than 2^8 (P <= 2^8
+//              otherwise), and writes the output row at the end;
+//   warp 4     TMA producer: one box per (page, 64-dim half) of K and of V;
+//   warp 5     allocates the tensor memory; lane 0 issues the MMAs:
+//              S_i = Q K_i^T  (M 128 rows, N 128 keys, K 128 dims), two S
+//              buffers so S_{i+1} runs while tile i is in softmax, and
+//              O += P_i V_i   (M 128 rows, N 128 dims, K 128 keys).
+//
+// Shared memory (1024-byte aligned, 128-byte swizzle everywhere, the layout
+// the MMA descriptors describe):
+//   Q  [2 dim halves][128 rows][64 bf16]       32 KiB
+//   P  [2 key halves][128 rows][64 bf16]       32 KiB
+//   stage s: K [2 dim halves][128 keys][64 bf16], V the same   2 x 64 KiB
+// Tensor memory: S buffers at columns 0 and 128, O at 256 (512 allocated).
+//
+// Every wait is bounded: on a timeout the CTA reports PKVQK_FLAG_WAIT_TIMEOUT,
+// lets its own copies and MMAs in flight finish (bounded), frees its tensor
+// memory and exits.
+#include "device_common.cuh"
+#include "prefill.h"
+#include "tc5.cuh"
+
+namespace pkvqk {
+
+namespace {
+
+constexpr int kM = 128;                        // rows per tile
+constexpr int kN = 128;                        // keys per tile
+constexpr int kHalf = 128 * 128;               // [128 rows][64 bf16] sub-tile, bytes
+constexpr int kTile = 2 * kHalf;               // [128 rows][128 bf16], bytes
+constexpr int kOffQ = 0;
+constexpr int kOffP = kTile;
+constexpr int kOffStage = 2 * kTile;
+constexpr int kStages = 2;
+constexpr int kStageBytes = 2 * kTile;         // K tile + V tile
+constexpr int kDataBytes = kOffStage + kStages * kStageBytes;
+constexpr int kThreads = 6 * 32;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Bars {
+  uint64_t full_k[kStages], full_v[kStages];     // TMA landed
+  uint64_t empty_k[kStages], empty_v[kStages];   // the MMAs reading a stage finished
+  uint64_t s_full[2], s_free[2];                 // S buffer written / read out
+  uint64_t p_full;                               // P written (and O rescaled)
+  uint64_t o_done;                               // O += P V finished
+  uint64_t drain;                                // MMA thread's own completion (timeout path)
+  uint32_t tmem_base;
+  int32_t abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+constexpr int kSmemBytes = kDataBytes + 256 + 1024;   // + barriers + alignment slack
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t s = smem_addr(p);
+  return p + (((s + 1023u) & ~1023u) - s);
+}
+
+// A [128 rows][128 bf16] operand stored as two 64-wide swizzled halves, read
+// K-major in 16-element steps: step kk is 32 bytes into the rows of half kk/4;
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_k_major(uint32_t tile, int kk) {
+  return tc5::smem_desc_sw128(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+}
+
+// V tile as the MN-major B operand of O += P V (N = dims, K = keys): 64 dims
+// per swizzled row, the two dim halves kHalf apart (leading offset), 8-key
+// groups 1024 bytes apart (stride offset); 16-key step ks starts 2048 bytes on.
+__device__ __forceinline__ uint64_t desc_v(uint32_t vtile, int ks) {
+  return tc5::smem_desc_sw128(vtile + ks * 2048, kHalf, 1024);
+}
+
+// 5-D tiled TMA load without an L2 hint: K/V tiles are read by every row tile
+// of their (sequence, kv head), so they should stay in L2 meanwhile.
+__device__ __forceinline__ void tma_load_5d_keep(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct Work {
+  int b, g, j, mt;
+  int L;         // keys of the sequence (clamped to the table)
+  int k0, k1;    // the split's key range
+  int key_end;   // keys at or past key_end are visible to no row of the tile
+  int ntiles;
+  int rows;      // q_len * group
+};
+
+__device__ Work decode_work(const PrefillArgs& a) {
+  Work w;
+  int x = blockIdx.x;
+  w.mt = x % a.m_tiles;
+  x /= a.m_tiles;
+  w.g = x % a.num_kv_heads;
+  w.j = x / a.num_kv_heads;
+  w.b = blockIdx.y;
+  const long long cap = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+  const long long L = min(static_cast<long long>(max(a.seq_lens[w.b], 0)), cap);
+  w.L = static_cast<int>(L);
+  const long long chunk_keys = static_cast<long long>(a.chunk_pages) * a.block_size;
+  w.k0 = static_cast<int>(min(L, w.j * chunk_keys));
+  w.k1 = (w.j == a.num_splits - 1) ? w.L : static_cast<int>(min(L, (w.j + 1) * chunk_keys));
+  w.rows = a.q_len * a.group;
+  const int last_row = min(w.mt * kM + kM - 1, w.rows - 1);
+  const int t_last = last_row / a.group;
+  w.key_end = max(w.k0, min(w.k1, w.L - a.q_len + t_last + 1));
+  w.ntiles = (w.key_end - w.k0 + kN - 1) / kN;
+  return w;
+}
+
+// ------------------------------------------------------------- producer
+
+__device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* kmap,
+                        const CUtensorMap* vmap, uint8_t* smem, Bars* bars, int* issued_out) {
+  const int lane = threadIdx.x & 31;
+  const int bs = a.block_size;
+  // slots per box: the largest power of two dividing the page size, at most
+  // a key tile; a tile's boxes start at multiples of it, so none crosses a page
+  const int tb = min(bs & -bs, kN);
+  const int ppt = kN / tb;                      // boxes per key tile
+  const int32_t* bt = a.block_tables + static_cast<long long>(w.b) * a.max_blocks_per_seq;
+  const int oob = static_cast<int>(a.num_blocks);   // past the extent: TMA fills zeros
+  int issued = 0;
+  for (int i = 0; i < w.ntiles; ++i) {
+    const int s = i & 1;
+    const uint32_t rel = ((i >> 1) - 1) & 1;         // release of tile i - 2
+    uint8_t* kt = smem + kOffStage + s * kStageBytes;
+    uint8_t* vt = kt + kTile;
+    int blk = oob, slot0 = 0;
+    if (lane < ppt) {
+      const int key = w.k0 + i * kN + lane * tb;   // first key of box `lane`
+      const int page = key / bs;
+      slot0 = key - page * bs;
+      if (key < w.key_end) {
+        const int id = __ldg(bt + page);
+        if (id >= 0 && static_cast<long long>(id) < a.num_blocks) blk = id;
+        else report(a.status_flags, kFlagBadBlock);
+      }
+    }
+    bool ok = true;
+    if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_k[s], rel);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        bars->abort = 1;
+        report(a.status_flags, kFlagTimeout);
+      }
+      break;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(&bars->full_k[s], kTile);
+    __syncwarp();
+    if (lane < ppt) {
+      tma_load_5d_keep(kt + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 0, w.g, blk);
+      tma_load_5d_keep(kt + kHalf + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 1, w.g,
+                       blk);
+    }
+    if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_v[s], rel);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        bars->abort = 1;
+        report(a.status_flags, kFlagTimeout);
+      }
+      issued = -(i + 1);                            // K of tile i is in flight, V is not
+      break;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[s], kTile);
+    __syncwarp();
+    if (lane < ppt) {
+      tma_load_5d_keep(vt + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 0, w.g, blk);
+      tma_load_5d_keep(vt + kHalf + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 1, w.g,
+                       blk);
+    }
+    issued = i + 1;
+  }
+  *issued_out = issued;
+}
+
+// After a timeout: wait (bounded) for the last copies issued into each stage.
+__device__ void drain_copies(Bars* bars, int issued) {
+  const bool v_missing = issued < 0;
+  const int n = v_missing ? -issued : issued;
+  for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i) {
+    const int s = i & 1;
+    mbar_wait(&bars->full_k[s], (i >> 1) & 1);
+    if (!(v_missing && i == n - 1)) mbar_wait(&bars->full_v[s], (i >> 1) & 1);
+  }
+}
+
+// ------------------------------------------------------------ MMA issue
+
+__device__ bool issue_pv(const Work& w, uint8_t* smem, Bars* bars, uint32_t tmem, int i) {
+  const int s = i & 1;
+  if (!mbar_wait(&bars->p_full, i & 1)) return false;
+  if (!mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
+  tc5::fence_after_sync();
+  const uint32_t p = smem_addr(smem + kOffP);
+  const uint32_t vt = smem_addr(smem + kOffStage + s * kStageBytes + kTile);
+  constexpr uint32_t idesc = tc5::idesc_bf16_f32(kM, kHeadDim, true);
+#pragma unroll
+  for (int ks = 0; ks < kN / 16; ++ks)
+    tc5::mma_f16(tmem + kColO, desc_k_major(p, ks), desc_v(vt, ks), idesc,
+                 (i > 0 || ks > 0) ? 1u : 0u);
+  tc5::commit(&bars->o_done);
+  tc5::commit(&bars->empty_v[s]);
+  return true;
+}
+
+__device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
+                           uint32_t tmem) {
+  const uint32_t q = smem_addr(smem + kOffQ);
+  constexpr uint32_t idesc = tc5::idesc_bf16_f32(kM, kN, false);
+  bool ok = true;
+  for (int i = 0; i < w.ntiles && ok; ++i) {
+    const int s = i & 1;
+    ok = mbar_wait(&bars->full_k[s], (i >> 1) & 1);
+    if (ok && i >= 2) ok = mbar_wait(&bars->s_free[s], ((i >> 1) - 1) & 1);
+    if (!ok) break;
+    tc5::fence_after_sync();
+    const uint32_t kt = smem_addr(smem + kOffStage + s * kStageBytes);
+#pragma unroll
+    for (int kk = 0; kk < kHeadDim / 16; ++kk)
+      tc5::mma_f16(tmem + kColS + s * kN, desc_k_major(q, kk), desc_k_major(kt, kk), idesc,
+                   kk > 0 ? 1u : 0u);
+    tc5::commit(&bars->s_full[s]);
+    tc5::commit(&bars->empty_k[s]);
+    if (i >= 1) ok = issue_pv(w, smem, bars, tmem, i - 1);
+  }
+  if (ok && w.ntiles > 0) ok = issue_pv(w, smem, bars, tmem, w.ntiles - 1);
+  if (!ok) {
+    bars->abort = 1;
+    report(a.status_flags, kFlagTimeout);
+    tc5::commit(&bars->drain);                 // everything issued so far ...
+    mbar_wait(&bars->drain, 0);                // ... has finished
+  }
+}
+
+// --------------------------------------------------------------- softmax
+
+__device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
+                             uint32_t tmem) {
+  const int r = threadIdx.x;                   // row of the tile = tensor-memory lane
+  const int warp = r >> 5, lane = r & 31;
+  const int rg = w.mt * kM + r;
+  const bool valid = rg < w.rows;
+  const int t = valid ? rg / a.group : 0;
+  const int hh = valid ? rg - t * a.group : 0;
+  // keys [k0, lim) are visible to this row
+  const int lim = valid ? max(w.k0, min(w.k1, w.L - a.q_len + t + 1)) : w.k0;
+  const uint32_t lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  uint8_t* p_tile = smem + kOffP;
+  const float sl2 = a.scale_log2;
+
+  float m_ref = -INFINITY;                     // reference max (log2 units) of P
+  float l = 0.f;                               // sum of P
+  bool ok = true;
+  for (int i = 0; i < w.ntiles; ++i) {
+    const int s = i & 1;
+    if (!warp_wait(&bars->s_full[s], (i >> 1) & 1)) {
+      ok = false;
+      break;
+    }
+    tc5::fence_after_sync();
+    float v[kN];
+#pragma unroll
+    for (int c = 0; c < kN / 32; ++c) tc5::tmem_ld32(lanes + kColS + s * kN + c * 32, v + c * 32);
+    tc5::wait_ld();
+    tc5::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->s_free[s]);
+
+    const int kb = w.k0 + i * kN;
+    const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kN; ++e)
+      if (e < nvis) mx = fmaxf(mx, v[e]);
+    const float m_tile = mx * sl2;
+    const bool grow = m_tile > m_ref + kRescaleLog2;
+    const float alpha = grow ? exp2f(m_ref - m_tile) : 1.f;
+    if (grow) m_ref = m_tile;
+
+    // O += P_{i-1} V_{i-1} must have finished before P is rewritten or O rescaled
+    if (i > 0) {
+      if (!warp_wait(&bars->o_done, (i - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+      if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+        for (int c = 0; c < kHeadDim / 32; ++c) {
+          float o[32];
+          tc5::tmem_ld32(lanes + kColO + c * 32, o);
+          tc5::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc5::tmem_st32(lanes + kColO + c * 32, o);
+        }
+        tc5::wait_st();
+      }
+    }
+    l *= alpha;
+    const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
+#pragma unroll
+    for (int kc = 0; kc < kN / 8; ++kc) {
+      float p[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = kc * 8 + e;
+        p[e] = (k < nvis) ? exp2f(fmaf(v[k], sl2, -u)) : 0.f;
+        l += p[e];
+      }
+      uint4 pk;
+      pk.x = pack_bf16x2(p[0], p[1]);
+      pk.y = pack_bf16x2(p[2], p[3]);
+      pk.z = pack_bf16x2(p[4], p[5]);
+      pk.w = pack_bf16x2(p[6], p[7]);
+      *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) = pk;
+    }
+    // Tail tile: cache slots past the last visible key may hold anything
+    // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
+    // their V rows are zeroed before the tensor core reads them.
+    if (kb + kN > w.key_end) {
+      if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (kb + r >= w.key_end) {
+        uint8_t* vrow = smem + kOffStage + s * kStageBytes + kTile + r * 128;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = z;
+          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
+        }
+      }
+    }
+    tc5::fence_smem_for_async();
+    tc5::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_full);
+  }
+  if (ok && w.ntiles > 0) {
+    ok = warp_wait(&bars->o_done, (w.ntiles - 1) & 1);
+    tc5::fence_after_sync();
+  }
+  if (!ok) {
+    bars->abort = 1;
+    report(a.status_flags, kFlagTimeout);
+    return;
+  }
+
+  const int h = w.g * a.group + hh;
+  const long long row = (static_cast<long long>(w.b) * a.q_len + t) * a.num_q_heads + h;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+  const bool have_o = w.ntiles > 0;            // uniform over the CTA
+  if (a.num_splits == 1) {
+    __nv_bfloat16* orow = a.out + row * kHeadDim;
+#pragma unroll 1
+    for (int c = 0; c < kHeadDim / 32; ++c) {
+      float o[32];
+      if (have_o) {
+        tc5::tmem_ld32(lanes + kColO + c * 32, o);
+        tc5::wait_ld();
+      }
+      if (valid) {
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint4 pk;
+          const float* x = o + q8 * 8;
+          pk.x = have_o ? pack_bf16x2(x[0] * inv, x[1] * inv) : 0u;
+          pk.y = have_o ? pack_bf16x2(x[2] * inv, x[3] * inv) : 0u;
+          pk.z = have_o ? pack_bf16x2(x[4] * inv, x[5] * inv) : 0u;
+          pk.w = have_o ? pack_bf16x2(x[6] * inv, x[7] * inv) : 0u;
+          *reinterpret_cast<uint4*>(orow + c * 32 + q8 * 8) = pk;
+        }
+      }
+    }
+    if (valid && a.lse_out != nullptr) a.lse_out[row] = lse;
+  } else {
+    const long long prow = row * a.num_splits + w.j;
+    float* po = a.ws_o + prow * kHeadDim;
+#pragma unroll 1
+    for (int c = 0; c < kHeadDim / 32; ++c) {
+      float o[32];
+      if (have_o) {
+        tc5::tmem_ld32(lanes + kColO + c * 32, o);
+        tc5::wait_ld();
+      }
+      if (valid) {
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float* x = o + q4 * 4;
+          *reinterpret_cast<float4*>(po + c * 32 + q4 * 4) =
+              have_o ? make_float4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+    if (valid) a.ws_lse[prow] = lse;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kDataBytes);
+  __shared__ int issued;
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == kProducerWarp * 32) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full_k[s], 1);
+      mbar_init(&bars->full_v[s], 1);
+      mbar_init(&bars->empty_k[s], 1);
+      mbar_init(&bars->empty_v[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 4);
+    }
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    issued = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
+
+  // launched as a programmatic dependent: q, the appended K/V, the tables and
+  // the lengths may come from the previous kernel in the stream
+  pdl_wait();
+  const Work w = decode_work(a);
+  if (warp < 4) {
+    // Q tile: row r = (token, q head of the group), two swizzled 64-dim halves
+    const int r = threadIdx.x;
+    const int rg = w.mt * kM + r;
+    const bool valid = rg < w.rows;
+    const int t = valid ? rg / a.group : 0;
+    const int hh = valid ? rg - t * a.group : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.q + (static_cast<long long>(w.b) * a.q_len + t) * a.q_stride_t +
+        static_cast<long long>(w.g * a.group + hh) * a.q_stride_h);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 x = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + kOffQ + (c >> 3) * kHalf + swz128(r, c & 7)) = x;
+    }
+    tc5::fence_smem_for_async();
+  }
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  pdl_launch_dependents();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+    softmax_rows(a, w, smem, bars, tmem);
+  } else if (warp == kProducerWarp) {
+    int n = 0;
+    produce(a, w, &kmap, &vmap, smem, bars, &n);
+    if (threadIdx.x == kProducerWarp * 32) issued = n;
+  } else {
+    if ((threadIdx.x & 31) == 0) issue_mmas(a, w, smem, bars, tmem);
+    __syncwarp();
+  }
+  tc5::fence_before_sync();
+  __syncthreads();
+  if (bars->abort && threadIdx.x == kProducerWarp * 32) drain_copies(bars, issued);
+  if (warp == kMmaWarp) {
+    tc5::fence_after_sync();
+    tc5::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int prefill_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const PrefillArgs& a, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long gx = static_cast<long long>(a.m_tiles) * a.num_kv_heads * a.num_splits;
+  return launch_pdl(paged_prefill_kernel, dim3(static_cast<unsigned>(gx), a.batch),
+                    dim3(kThreads), kSmemBytes, stream, kmap, vmap, a);
+}
+
+}  // namespace pkvqk

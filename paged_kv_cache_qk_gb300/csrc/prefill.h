@@ -1,0 +1,40 @@
+// Internal launch interface of the multi-query (chunked-prefill) attention
+// kernel.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkvqk {
+
+struct PrefillArgs {
+  const __nv_bfloat16* q;          // [B, q_len, Hq, 128] (strided tokens / heads)
+  int64_t q_stride_t, q_stride_h;
+  const int32_t* block_tables;     // [B, max_blocks_per_seq]
+  int32_t max_blocks_per_seq;
+  const int32_t* seq_lens;         // [B], counting the q_len new tokens
+  int32_t batch, q_len, num_q_heads, num_kv_heads, group;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t num_splits;              // >= 1
+  int32_t chunk_pages;             // pages per split
+  int32_t m_tiles;                 // ceil(q_len * group / 128)
+  float scale_log2;                // softmax scale * log2(e)
+  __nv_bfloat16* out;              // num_splits == 1: [B, q_len, Hq, 128]
+  float* lse_out;                  // num_splits == 1: optional [B, q_len, Hq]
+  float* ws_o;                     // num_splits > 1: [rows, S, 128] normalised partials
+  float* ws_lse;                   // num_splits > 1: [rows, S]
+  int32_t* status_flags;
+};
+
+// Shared-memory bytes one CTA of the kernel takes (one CTA per SM).
+int prefill_smem_bytes();
+
+// Tensor maps: 5-D cache views with a box of (64 dims, b slots, 1 half, 1 head,
+// 1 block), b = the largest power of two dividing block_size, at most 128.
+cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace pkvqk

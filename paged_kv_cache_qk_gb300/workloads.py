@@ -18,6 +18,10 @@ PR #585, Qwen3-0.6B / 1.7B; InfiniLM issue #498, Qwen3-30B-A3B with
                         pages needed, shuffled block ids.
 * ``verify_causal``     16q/8kv, D=128, batch 32, 5 query tokens per sequence
                         (k = 4 draft tokens + 1), prior context U[2048, 8192].
+* ``chunked_prefill``   16q/8kv, D=128, batch 8, a chunk of 512 new tokens per
+                        sequence after a prior context U[0, 6144] (the chunks
+                        of a ~6.5k-token prompt, the size the pages inject in
+                        their decode-stall workload).
 
 Every tensor is drawn from a generator seeded per problem.  Host-side values
 that a scheduler knows without touching the device (sequence lengths, block
@@ -196,3 +200,16 @@ def verify_causal(device="cpu", seed=BASE_SEED + 4, batch=32, q_len=5,
     nb = int(sum(_pages(n, 16) for n in seq_lens))
     return make_problem(f"verify_causal_b{batch}_k{q_len - 1}", 16, 8, 128, 16,
                         seq_lens, q_len, nb, seed, device)
+
+
+def chunked_prefill(device="cpu", seed=BASE_SEED + 5, batch=8, chunk=512, lo=0, hi=6144,
+                    Hq=16, Hkv=8, block_size=16, extra_blocks=0):
+    """16q/8kv, D=128: `chunk` new tokens per sequence after a prior context
+    U[lo, hi] (0 = the prompt's first chunk); cache = the pages needed plus
+    `extra_blocks`, shuffled block ids."""
+    rng = np.random.default_rng(seed)
+    prior = rng.integers(lo, hi + 1, size=batch)
+    seq_lens = prior + chunk
+    nb = int(sum(_pages(n, block_size) for n in seq_lens)) + extra_blocks
+    return make_problem(f"chunked_prefill_b{batch}_c{chunk}", Hq, Hkv, 128, block_size,
+                        seq_lens, chunk, nb, seed, device)

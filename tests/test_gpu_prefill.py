@@ -1,0 +1,197 @@
+"""GPU parity of pkvqk_paged_prefill (tcgen05 multi-query attention) against
+the fp64 oracle.
+
+Operation: InfiniLM PR #585, section "概述 / Summary", item 4 (chunked
+prefill; the verify step's fixed b x (k+1) shape) over the paged cache of
+item 1: new token t of a sequence attends causally to every key up to its own
+position.  Small cases compare every row; the benchmark-sized chunked-prefill
+workload compares sampled tokens, each against the oracle's decode of that
+token (query t of a q_len chunk sees exactly the keys a single query at
+seq_len - q_len + t + 1 sees, a property the oracle's own pins check).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_qk_gb300 import workloads
+from tests._parity import (assert_attention_close, bits, compact_cache, oracle_attention)
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(lib, p, num_splits=1, hint=None, q=None, k_cache=None, v_cache=None, flags=None,
+             scale=0.0):
+    q = p.q if q is None else q
+    k_cache = p.k_cache if k_cache is None else k_cache
+    v_cache = p.v_cache if v_cache is None else v_cache
+    out = torch.full((p.B, p.q_len, p.Hq, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.B, p.q_len, p.Hq), float("nan"), device="cuda")
+    hint = p.max_seq_len if hint is None else hint
+    nbytes = lib.prefill_workspace_bytes(p.B, p.q_len, p.Hq, p.D, num_splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    lib.paged_prefill(q, k_cache, v_cache, p.block_tables, p.seq_lens, out, q_len=p.q_len,
+                      num_splits=num_splits, max_seq_len_hint=hint, scale=scale, lse_out=lse,
+                      workspace=ws, status_flags=flags)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _problem(Hq, Hkv, q_len, bs, priors, seed, extra_blocks=0):
+    seq_lens = np.asarray(priors, np.int64) + q_len
+    nb = int(sum(-(-int(n) // bs) for n in seq_lens)) + extra_blocks
+    return workloads.make_problem(f"prefill_{Hq}_{Hkv}_{q_len}_{bs}", Hq, Hkv, 128, bs, seq_lens,
+                                  q_len, max(nb, 1), seed, "cuda")
+
+
+def _check_all(p, out, lse, what, scale=None):
+    ref, ref_lse = oracle_attention(p, bits(p.q), scale=scale)
+    return assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, what)
+
+
+# (Hq, Hkv, q_len, block_size, priors): row tiles of 128 packed (token, head)
+# rows -- exact, ragged, several per kv head; fresh prompts (prior 0), short
+# and long priors; GQA groups 1, 2, 8; page sizes 16 .. 256 and a
+# non-power-of-two 48
+CASES = [
+    (16, 8, 64, 16, [0, 100, 300]),
+    (16, 8, 200, 16, [37, 0, 513]),
+    (32, 4, 40, 32, [250, 1]),
+    (16, 16, 130, 64, [0, 700]),
+    (16, 8, 33, 256, [300, 5]),
+    (16, 8, 50, 48, [61, 190]),
+    (16, 8, 5, 16, [2000, 17, 0]),
+    (16, 8, 1, 16, [900, 0, 31]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"Hq{c[0]}-Hkv{c[1]}-T{c[2]}-bs{c[3]}")
+def test_prefill_all_rows_match_oracle(lib, case):
+    Hq, Hkv, q_len, bs, priors = case
+    p = _problem(Hq, Hkv, q_len, bs, priors, seed=900 + q_len + bs)
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = _prefill(lib, p, flags=flags)
+    assert flags.item() == 0
+    _check_all(p, out, lse, f"prefill {case}")
+
+
+@pytest.mark.parametrize("S", [2, 3, 7])
+def test_prefill_splits_match_oracle(lib, S):
+    p = _problem(16, 8, 96, 16, [1500, 40, 0, 777], seed=31 + S)
+    out, lse = _prefill(lib, p, num_splits=S)
+    _check_all(p, out, lse, f"prefill S={S}")
+
+
+def test_prefill_short_hint_last_split_takes_the_rest(lib):
+    # a hint below the longest sequence: the last split covers every key past
+    # (S-1) * C pages, so nothing is dropped
+    p = _problem(16, 8, 20, 16, [1000, 300], seed=5)
+    out, lse = _prefill(lib, p, num_splits=4, hint=200)
+    _check_all(p, out, lse, "short hint")
+
+
+def test_prefill_custom_scale(lib):
+    p = _problem(16, 8, 24, 16, [300, 10], seed=8)
+    out, lse = _prefill(lib, p, scale=0.05)
+    _check_all(p, out, lse, "scale 0.05", scale=0.05)
+
+
+def test_prefill_equals_verify_decode_kernel(lib):
+    """q_len 5 (the verify shape): the tensor-core kernel and the decode
+    kernel's verify path both match the oracle and each other closely."""
+    p = workloads.verify_causal(device="cuda", batch=6)
+    out_p, lse_p = _prefill(lib, p)
+    out_d = torch.empty_like(out_p)
+    lse_d = torch.empty_like(lse_p)
+    lib.paged_decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out_d, q_len=p.q_len,
+                     num_splits=1, max_seq_len_hint=p.max_seq_len, lse_out=lse_d)
+    torch.cuda.synchronize()
+    _check_all(p, out_p, lse_p, "verify via prefill")
+    diff = (out_p.float() - out_d.float()).abs()
+    assert diff.max().item() <= 2e-2
+    assert (lse_p - lse_d).abs().max().item() <= 1e-3
+
+
+def test_prefill_rows_without_keys(lib):
+    # seq_len below q_len (tokens whose position would be negative) and an
+    # empty sequence: their rows see no key -> 0 output and lse = -inf
+    p = _problem(16, 8, 8, 16, [0, 0], seed=12)
+    p.seq_lens = torch.tensor([3, 0], dtype=torch.int32, device="cuda")
+    p.seq_lens_host = np.array([3, 0], np.int64)
+    out, lse = _prefill(lib, p, hint=8)
+    ref, ref_lse = oracle_attention(p, bits(p.q))
+    got = oracle.bf16_bits_to_f64(bits(out))
+    empty = np.isneginf(ref_lse)
+    assert empty.sum() == (5 + 8) * 16
+    assert np.array_equal(np.isneginf(lse.cpu().numpy()), empty)
+    assert np.all(got[empty] == 0.0)
+    assert np.abs(got[~empty] - ref[~empty]).max() <= 2e-2
+
+
+def test_prefill_ignores_non_finite_slots_past_the_end(lib):
+    """Cache slots past a sequence's last key (the rest of its last page) may
+    hold anything, NaN included; they must not reach the output."""
+    p = _problem(16, 8, 40, 16, [100, 7], seed=21)
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    for b in range(p.B):
+        L = int(p.seq_lens_host[b])
+        last = int(p.block_tables_host[b, (L - 1) // 16])
+        kc[last, L % 16 or 16:] = float("nan")
+        vc[last, L % 16 or 16:] = float("nan")
+    out, lse = _prefill(lib, p, k_cache=kc, v_cache=vc)
+    ref, ref_lse = oracle_attention(p, bits(p.q), k_cache=kc, v_cache=vc)
+    assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "nan tail")
+
+
+def test_prefill_bad_block_id_is_flagged_and_reads_zeros(lib):
+    p = _problem(16, 8, 16, 16, [64], seed=3, extra_blocks=4)
+    bt = p.block_tables.clone()
+    bt[0, 1] = p.num_blocks + 10                       # keys 16..31 -> zeros
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
+    lib.paged_prefill(p.q, p.k_cache, p.v_cache, bt, p.seq_lens, out, q_len=p.q_len,
+                      max_seq_len_hint=p.max_seq_len, status_flags=flags)
+    torch.cuda.synchronize()
+    assert flags.item() & lib.FLAG_BAD_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    # the oracle on a cache whose block 1 of the sequence is zero gives the same
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    blk = int(p.block_tables_host[0, 1])
+    kc[blk] = 0
+    vc[blk] = 0
+    ref, _ = oracle_attention(p, bits(p.q), k_cache=kc, v_cache=vc)
+    assert_attention_close(bits(out), ref, what="bad block")
+
+
+def test_prefill_chunked_workload_sampled(lib):
+    """The benchmark workload (8 sequences x 512-token chunks after prior
+    context U[0, 6144]) in the benchmark's launch configuration; sampled
+    tokens of every sequence against the oracle's decode of that token."""
+    p = workloads.chunked_prefill(device="cuda")
+    S = lib.choose_prefill_splits(p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
+    out, lse = _prefill(lib, p, num_splits=S)
+    rng = np.random.default_rng(44)
+    qb = bits(p.q).reshape(p.B, p.q_len, p.Hq, p.D)
+    kb, vb, table, lens = compact_cache(p, list(range(p.B)))
+    for b in range(p.B):
+        for t in sorted(set([0, p.q_len - 1] + list(rng.integers(0, p.q_len, 2)))):
+            ctx = int(lens[b]) - p.q_len + t + 1
+            ref, ref_lse = oracle.paged_attention(qb[b:b + 1, t:t + 1], kb, vb, table[b:b + 1],
+                                                  np.array([ctx]), p.block_size)
+            assert_attention_close(bits(out[b:b + 1, t:t + 1]), ref,
+                                   lse[b:b + 1, t:t + 1].cpu().numpy(), ref_lse,
+                                   f"chunked b={b} t={t}")
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    p = _problem(16, 8, 8, 16, [10], seed=1)
+    out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.PkvqkError) as e:
+        lib.paged_prefill(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                          q_len=p.q_len, num_splits=0)
+    assert e.value.status == lib.PKVQK_ERR_INVALID_ARG
+    with pytest.raises(lib.PkvqkError) as e:
+        lib.paged_prefill(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                          q_len=p.q_len, num_splits=3)       # no workspace
+    assert e.value.status == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
