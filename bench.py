@@ -51,6 +51,24 @@ WORKLOADS = {
 }
 WORKLOADS["decode_gqa8_64x4096"] = ("make_problem_uniform_gqa8", {},
                                     "GQA-8 decode 32q/4kv D128 bs16, batch 64 x ctx 4096 (uniform)")
+# the tensor-core multi-query kernel (pkvqk_paged_prefill): chunked prefill,
+# and the verify shape through the same kernel
+PREFILL_WORKLOADS = {
+    "prefill_8x512": ("chunked_prefill", {},
+                      "chunked prefill 16q/8kv D128 bs16, batch 8 x 512-token chunk, "
+                      "prior context U[0, 6144]"),
+    "prefill_4x2048": ("chunked_prefill", {"batch": 4, "chunk": 2048, "lo": 0, "hi": 8192},
+                       "chunked prefill 16q/8kv D128 bs16, batch 4 x 2048-token chunk, "
+                       "prior context U[0, 8192]"),
+    "prefill_gqa8_8x512": ("chunked_prefill", {"Hq": 32, "Hkv": 4},
+                           "chunked prefill 32q/4kv D128 bs16, batch 8 x 512-token chunk, "
+                           "prior context U[0, 6144]"),
+    "verify_32x5_tc": ("verify_causal", {},
+                       "speculative verify 16q/8kv D128 bs16, batch 32, 5 query tokens, prior "
+                       "U[2048,8192], on the tensor-core multi-query kernel"),
+}
+WORKLOADS.update(PREFILL_WORKLOADS)
+PREFILL_METRIC = "causal multi-query paged attention achieved TFLOP/s (% of measured bf16 peak)"
 for _b in (1, 8, 32, 64):
     for _c in (512, 2048, 8192):
         WORKLOADS.setdefault(f"decode_{_b}x{_c}", ("decode_uniform", {"batch": _b, "ctx": _c},
@@ -77,14 +95,26 @@ def kernel_src_hash():
     return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
 
 
-def load_peaks():
+def load_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
+
+
+def attention_flops(p):
+    """Algorithmic FLOPs of the causal attention: per visible (query token,
+    key) pair and q head, 2*D for q.k and 2*D for p*v."""
+    T = p.q_len
+    n = 0
+    for L in p.seq_lens_host:
+        L = int(L)
+        # token t sees L - T + t + 1 keys (clipped at 0)
+        n += sum(max(0, L - T + t + 1) for t in range(T))
+    return 4 * p.D * p.Hq * n
 
 
 def step_bytes(p):
@@ -291,9 +321,15 @@ def main():
         p = getattr(workloads, builder)(device=dev, **kw)
     decode_bytes, append_bytes = step_bytes(p)
     rows_per_kv = p.q_len * p.Hq // p.Hkv
-    S = args.num_splits if args.num_splits >= 0 else lib.choose_num_splits(
-        p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
-    ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+    prefill = args.workload in PREFILL_WORKLOADS
+    if prefill:
+        S = args.num_splits if args.num_splits >= 1 else lib.choose_prefill_splits(
+            p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
+        ws_bytes = lib.prefill_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+    else:
+        S = args.num_splits if args.num_splits >= 0 else lib.choose_num_splits(
+            p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
+        ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if ws_bytes else None
     out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev)
     q = p.q.clone()
@@ -303,8 +339,14 @@ def main():
     flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
 
     def decode_call(qq, bt, sl):
-        lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len, num_splits=S,
-                         max_seq_len_hint=p.max_seq_len, workspace=ws, stream=stream)
+        if prefill:
+            lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len,
+                              num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
+                              stream=stream)
+        else:
+            lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len,
+                             num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
+                             stream=stream)
 
     def step(ev=None):
         if ev is not None:
@@ -317,7 +359,10 @@ def main():
         if ev is not None:
             ev[2].record(stream)
 
-    launches_per_step = 2 + (1 if S == 0 else 0)     # append, decode (+ balanced combine)
+    if prefill:   # append, prefill (+ lse combine when split)
+        launches_per_step = 2 + (1 if S > 1 else 0)
+    else:         # append, decode (+ balanced combine)
+        launches_per_step = 2 + (1 if S == 0 else 0)
 
     for _ in range(args.warmup):
         step()
@@ -461,7 +506,35 @@ def main():
         "append_avg_ms": round(statistics.fmean(append_ms), 5),
         "e2e_gpu_launches": K_e2e * launches_per_step,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if prefill:
+        flops = attention_flops(p)
+        tpeak, tpeak_kind = load_peaks("bf16_tflops", 1900.0)
+        tflops = flops / (dec_avg_ms * 1e-3) / 1e12
+        line["metric"] = PREFILL_METRIC
+        line["value"] = round(world * flops / (ms * 1e-3) / 1e12, 2)
+        line["unit"] = "TFLOP/s"
+        line["e2e"]["value"] = round(world * flops / (e2e_ms * 1e-3) / 1e12, 2)
+        line["e2e"]["unit"] = "TFLOP/s"
+        line["config"]["schedule"] = f"row tiles of 128 x split {S}"
+        line["config"]["flops_per_step"] = flops
+        line["config"]["kv_bytes_per_step"] = decode_bytes
+        del line["pct_of_nominal_8tbs"]
+        line["tokens_per_s"] = round(world * p.T / (ms * 1e-3), 1)
+        line["roofline"] = {
+            "kernel": "pkvqk_paged_prefill call: paged_prefill_kernel"
+                      + (" + lse_combine_kernel" if S > 1 else ""),
+            "bound": "tensor",
+            "achieved": round(tflops, 2),
+            "peak": tpeak,
+            "peak_kind": tpeak_kind + " (bf16 burst)",
+            "unit": "TFLOP/s",
+            "frac": round(tflops / tpeak, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "avg_launch_ms": round(dec_avg_ms, 5),
+            "hbm_gbs_of_kv": round(achieved, 2),
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not prefill:
         cb = run_cpu_baseline_child(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)
         if "error" in cb:
             line["cpu_baseline"] = {"error": cb["error"]}

@@ -272,6 +272,60 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
 
 // --------------------------------------------------------------- softmax
 
+// 2^x on the SFU (relative error ~2^-22; -inf -> +0).  P is rounded to bf16
+// right after, so the approximate unit is accurate enough.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Max of the visible scores of a row (keys e < nvis of the tile), eight
+// independent chains.
+template <bool kMasked>
+__device__ __forceinline__ float row_max(const float (&v)[kN], int nvis) {
+  float m[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < kN; ++e)
+    if (!kMasked || e < nvis) m[e & 7] = fmaxf(m[e & 7], v[e]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], m[j + 4]);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere), written as
+// bf16 to row r of the swizzled P tile; returns the row's sum of P.
+template <bool kMasked>
+__device__ __forceinline__ float write_p(const float (&v)[kN], int nvis, float sl2, float u,
+                                         uint8_t* p_tile, int r) {
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  const float nu = -u;
+#pragma unroll
+  for (int kc = 0; kc < kN / 8; ++kc) {
+    float p[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int k = kc * 8 + e;
+      p[e] = ex2_approx(fmaf(v[k], sl2, nu));
+      if (kMasked) p[e] = (k < nvis) ? p[e] : 0.f;
+      acc[e] += p[e];
+    }
+    uint4 pk;
+    pk.x = pack_bf16x2(p[0], p[1]);
+    pk.y = pack_bf16x2(p[2], p[3]);
+    pk.z = pack_bf16x2(p[4], p[5]);
+    pk.w = pack_bf16x2(p[6], p[7]);
+    *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) = pk;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] += acc[j + 4];
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
                              uint32_t tmem) {
   const int r = threadIdx.x;                   // row of the tile = tensor-memory lane
@@ -306,13 +360,12 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
 
     const int kb = w.k0 + i * kN;
     const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
-    float mx = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < kN; ++e)
-      if (e < nvis) mx = fmaxf(mx, v[e]);
+    // interior tiles (every row of the warp sees all 128 keys) skip the masks
+    const bool whole = __all_sync(0xffffffffu, nvis == kN);
+    const float mx = whole ? row_max<false>(v, nvis) : row_max<true>(v, nvis);
     const float m_tile = mx * sl2;
     const bool grow = m_tile > m_ref + kRescaleLog2;
-    const float alpha = grow ? exp2f(m_ref - m_tile) : 1.f;
+    const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
     if (grow) m_ref = m_tile;
 
     // O += P_{i-1} V_{i-1} must have finished before P is rewritten or O rescaled
@@ -335,24 +388,9 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
         tc5::wait_st();
       }
     }
-    l *= alpha;
     const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
-#pragma unroll
-    for (int kc = 0; kc < kN / 8; ++kc) {
-      float p[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int k = kc * 8 + e;
-        p[e] = (k < nvis) ? exp2f(fmaf(v[k], sl2, -u)) : 0.f;
-        l += p[e];
-      }
-      uint4 pk;
-      pk.x = pack_bf16x2(p[0], p[1]);
-      pk.y = pack_bf16x2(p[2], p[3]);
-      pk.z = pack_bf16x2(p[4], p[5]);
-      pk.w = pack_bf16x2(p[6], p[7]);
-      *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) = pk;
-    }
+    l = l * alpha + (whole ? write_p<false>(v, nvis, sl2, u, p_tile, r)
+                           : write_p<true>(v, nvis, sl2, u, p_tile, r));
     // Tail tile: cache slots past the last visible key may hold anything
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
     // their V rows are zeroed before the tensor core reads them.
