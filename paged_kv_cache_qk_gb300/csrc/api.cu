@@ -346,7 +346,8 @@ pkvqk_status run_prefill(const DecodeCall& c) {
     return fail(PKVQK_ERR_INVALID_ARG, "q strides must be multiples of 8 elements");
   if (!std::isfinite(c.scale)) return fail(PKVQK_ERR_INVALID_ARG, "scale is not finite");
   const int S = c.num_splits;
-  const int m_tiles = static_cast<int>((rows + 127) / 128);
+  const int m_tiles = static_cast<int>((rows + pkvqk::kPrefillRowsPerCta - 1) /
+                                       pkvqk::kPrefillRowsPerCta);
   const int64_t grid_x = static_cast<int64_t>(m_tiles) * L.num_kv_heads * S;
   if (grid_x > INT32_MAX) return fail(PKVQK_ERR_UNSUPPORTED, "too many CTAs (%lld)",
                                       static_cast<long long>(grid_x));
@@ -610,7 +611,8 @@ int32_t pkvqk_choose_prefill_splits(int32_t batch, int32_t num_kv_heads, int32_t
                                     int32_t group, int32_t max_seq_len, int32_t sm_count) {
   if (batch <= 0 || num_kv_heads <= 0 || q_len <= 0 || group <= 0 || max_seq_len <= 0) return 1;
   if (sm_count <= 0) sm_count = sm_count_current();
-  const int64_t m_tiles = (static_cast<int64_t>(q_len) * group + 127) / 128;
+  const int64_t m_tiles = (static_cast<int64_t>(q_len) * group + pkvqk::kPrefillRowsPerCta - 1) /
+                          pkvqk::kPrefillRowsPerCta;
   const int64_t ctas = static_cast<int64_t>(batch) * num_kv_heads * m_tiles;
   if (ctas >= sm_count) return 1;
   int64_t S = (sm_count + ctas - 1) / ctas;

@@ -11,27 +11,33 @@
 // the block table; q head h reads kv head h / group; softmax scale D^-1/2
 // unless the caller gives one.
 //
-// One CTA = one tile of 128 packed rows r = t * group + (h % group) of one
-// (sequence, kv head), restricted to one split of the key range.  Keys stream
-// in tiles of 128 through a two-stage ring (K and V released separately).
-// Warp roles:
-//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r).  Reads its
-//              score row S = Q K^T from tensor memory, keeps the running max
-//              and sum, writes P (bf16) to shared memory, rescales O in tensor
-//              memory only when the max grew by more than 2^8 (P <= 2^8
-//              otherwise), and writes the output row at the end;
-//   warp 4     TMA producer: one box per (page, 64-dim half) of K and of V;
-//   warp 5     allocates the tensor memory; lane 0 issues the MMAs:
-//              S_i = Q K_i^T  (M 128 rows, N 128 keys, K 128 dims), two S
-//              buffers so S_{i+1} runs while tile i is in softmax, and
-//              O += P_i V_i   (M 128 rows, N 128 dims, K 128 keys).
+// One CTA = two tiles A and B of 128 packed rows r = t * group + (h % group)
+// of one (sequence, kv head) -- 256 consecutive rows -- restricted to one
+// split of the key range.  Keys stream in tiles of 128 through two-stage TMA
+// rings (K and V separately); both row tiles use every key tile, and the
+// tensor core alternates between them so that one tile's softmax runs while
+// the other tile's MMAs do (ping-pong).  Warp roles:
+//   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (tensor-memory
+//              lane r).  Reads its score row S = Q K^T from tensor memory,
+//              keeps the running max and sum, writes P (bf16) to the shared P
+//              buffer when it is free, rescales O in tensor memory only when
+//              the max grew by more than 2^8 (P <= 2^8 otherwise), and writes
+//              the output row at the end;
+//   warp 8     TMA producer: one box per (page, 64-dim half) of K and of V;
+//   warp 9     allocates the tensor memory; lane 0 issues the MMAs in the
+//              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
+//              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims),
+//              O_x += P_x V_i   (M 128 rows, N 128 dims, K 128 keys).
+// The single P buffer passes A -> B -> A: softmax B writes P_B(i) once
+// PV_A(i) finished, softmax A writes P_A(i+1) once PV_B(i) finished.
 //
 // Shared memory (1024-byte aligned, 128-byte swizzle everywhere, the layout
 // the MMA descriptors describe):
-//   Q  [2 dim halves][128 rows][64 bf16]       32 KiB
-//   P  [2 key halves][128 rows][64 bf16]       32 KiB
-//   stage s: K [2 dim halves][128 keys][64 bf16], V the same   2 x 64 KiB
-// Tensor memory: S buffers at columns 0 and 128, O at 256 (512 allocated).
+//   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]      2 x 32 KiB
+//   P         [2 key halves][128 rows][64 bf16]      32 KiB
+//   K stage s [2 dim halves][128 keys][64 bf16]      2 x 32 KiB
+//   V stage s  the same                              2 x 32 KiB
+// Tensor memory: S_A at columns 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 //
 // Every wait is bounded: on a timeout the CTA reports PKVQK_FLAG_WAIT_TIMEOUT,
 // lets its own copies and MMAs in flight finish (bounded), frees its tensor
@@ -44,31 +50,32 @@ namespace pkvqk {
 
 namespace {
 
-constexpr int kM = 128;                        // rows per tile
-constexpr int kN = 128;                        // keys per tile
+constexpr int kM = 128;                        // rows per row tile
+constexpr int kN = 128;                        // keys per key tile
+static_assert(2 * kM == kPrefillRowsPerCta, "two row tiles per CTA");
 constexpr int kHalf = 128 * 128;               // [128 rows][64 bf16] sub-tile, bytes
 constexpr int kTile = 2 * kHalf;               // [128 rows][128 bf16], bytes
-constexpr int kOffQ = 0;
-constexpr int kOffP = kTile;
-constexpr int kOffStage = 2 * kTile;
 constexpr int kStages = 2;
-constexpr int kStageBytes = 2 * kTile;         // K tile + V tile
-constexpr int kDataBytes = kOffStage + kStages * kStageBytes;
-constexpr int kThreads = 6 * 32;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kOffQ = 0;                       // Q_A, Q_B
+constexpr int kOffP = 2 * kTile;
+constexpr int kOffK = 3 * kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kDataBytes = kOffV + kStages * kTile;
+constexpr int kThreads = 10 * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColS = 0;                  // + x * kN
+constexpr uint32_t kColO = 256;                // + x * kN
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Bars {
   uint64_t full_k[kStages], full_v[kStages];     // TMA landed
   uint64_t empty_k[kStages], empty_v[kStages];   // the MMAs reading a stage finished
-  uint64_t s_full[2], s_free[2];                 // S buffer written / read out
-  uint64_t p_full;                               // P written (and O rescaled)
-  uint64_t o_done;                               // O += P V finished
+  uint64_t s_full[2];                            // S_x written
+  uint64_t p_full[2];                            // P_x written (and O_x rescaled)
+  uint64_t pv_done[2];                           // O_x += P_x V finished
   uint64_t drain;                                // MMA thread's own completion (timeout path)
   uint32_t tmem_base;
   int32_t abort;
@@ -116,9 +123,10 @@ struct Work {
   int b, g, j, mt;
   int L;         // keys of the sequence (clamped to the table)
   int k0, k1;    // the split's key range
-  int key_end;   // keys at or past key_end are visible to no row of the tile
+  int key_end;   // keys at or past key_end are visible to no row of the CTA
   int ntiles;
   int rows;      // q_len * group
+  bool has_b;    // row tile B holds rows
 };
 
 __device__ Work decode_work(const PrefillArgs& a) {
@@ -136,7 +144,9 @@ __device__ Work decode_work(const PrefillArgs& a) {
   w.k0 = static_cast<int>(min(L, w.j * chunk_keys));
   w.k1 = (w.j == a.num_splits - 1) ? w.L : static_cast<int>(min(L, (w.j + 1) * chunk_keys));
   w.rows = a.q_len * a.group;
-  const int last_row = min(w.mt * kM + kM - 1, w.rows - 1);
+  const int row0 = w.mt * 2 * kM;
+  w.has_b = row0 + kM < w.rows;
+  const int last_row = min(row0 + 2 * kM - 1, w.rows - 1);
   const int t_last = last_row / a.group;
   w.key_end = max(w.k0, min(w.k1, w.L - a.q_len + t_last + 1));
   w.ntiles = (w.key_end - w.k0 + kN - 1) / kN;
@@ -159,8 +169,8 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
   for (int i = 0; i < w.ntiles; ++i) {
     const int s = i & 1;
     const uint32_t rel = ((i >> 1) - 1) & 1;         // release of tile i - 2
-    uint8_t* kt = smem + kOffStage + s * kStageBytes;
-    uint8_t* vt = kt + kTile;
+    uint8_t* kt = smem + kOffK + s * kTile;
+    uint8_t* vt = smem + kOffV + s * kTile;
     int blk = oob, slot0 = 0;
     if (lane < ppt) {
       const int key = w.k0 + i * kN + lane * tb;   // first key of box `lane`
@@ -224,44 +234,54 @@ __device__ void drain_copies(Bars* bars, int issued) {
 
 // ------------------------------------------------------------ MMA issue
 
-__device__ bool issue_pv(const Work& w, uint8_t* smem, Bars* bars, uint32_t tmem, int i) {
-  const int s = i & 1;
-  if (!mbar_wait(&bars->p_full, i & 1)) return false;
-  if (!mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
-  tc5::fence_after_sync();
-  const uint32_t p = smem_addr(smem + kOffP);
-  const uint32_t vt = smem_addr(smem + kOffStage + s * kStageBytes + kTile);
-  constexpr uint32_t idesc = tc5::idesc_bf16_f32(kM, kHeadDim, true);
-#pragma unroll
-  for (int ks = 0; ks < kN / 16; ++ks)
-    tc5::mma_f16(tmem + kColO, desc_k_major(p, ks), desc_v(vt, ks), idesc,
-                 (i > 0 || ks > 0) ? 1u : 0u);
-  tc5::commit(&bars->o_done);
-  tc5::commit(&bars->empty_v[s]);
-  return true;
-}
-
 __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
                            uint32_t tmem) {
-  const uint32_t q = smem_addr(smem + kOffQ);
-  constexpr uint32_t idesc = tc5::idesc_bf16_f32(kM, kN, false);
-  bool ok = true;
-  for (int i = 0; i < w.ntiles && ok; ++i) {
+  const int last = w.has_b ? 1 : 0;            // the row tile that reads a stage last
+  const uint32_t p = smem_addr(smem + kOffP);
+  constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(kM, kN, false);
+  constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kM, kHeadDim, true);
+  // S_x(i) = Q_x K_i^T
+  auto mma_s = [&](int x, int i) -> bool {
     const int s = i & 1;
-    ok = mbar_wait(&bars->full_k[s], (i >> 1) & 1);
-    if (ok && i >= 2) ok = mbar_wait(&bars->s_free[s], ((i >> 1) - 1) & 1);
-    if (!ok) break;
+    if (x == 0 && !mbar_wait(&bars->full_k[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
-    const uint32_t kt = smem_addr(smem + kOffStage + s * kStageBytes);
+    const uint32_t q = smem_addr(smem + kOffQ + x * kTile);
+    const uint32_t kt = smem_addr(smem + kOffK + s * kTile);
 #pragma unroll
     for (int kk = 0; kk < kHeadDim / 16; ++kk)
-      tc5::mma_f16(tmem + kColS + s * kN, desc_k_major(q, kk), desc_k_major(kt, kk), idesc,
+      tc5::mma_f16(tmem + kColS + x * kN, desc_k_major(q, kk), desc_k_major(kt, kk), idesc_s,
                    kk > 0 ? 1u : 0u);
-    tc5::commit(&bars->s_full[s]);
-    tc5::commit(&bars->empty_k[s]);
-    if (i >= 1) ok = issue_pv(w, smem, bars, tmem, i - 1);
+    tc5::commit(&bars->s_full[x]);
+    if (x == last) tc5::commit(&bars->empty_k[s]);
+    return true;
+  };
+  // O_x += P_x V_i
+  auto mma_pv = [&](int x, int i) -> bool {
+    const int s = i & 1;
+    if (!mbar_wait(&bars->p_full[x], i & 1)) return false;
+    if (x == 0 && !mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
+    tc5::fence_after_sync();
+    const uint32_t vt = smem_addr(smem + kOffV + s * kTile);
+#pragma unroll
+    for (int ks = 0; ks < kN / 16; ++ks)
+      tc5::mma_f16(tmem + kColO + x * kN, desc_k_major(p, ks), desc_v(vt, ks), idesc_pv,
+                   (i > 0 || ks > 0) ? 1u : 0u);
+    tc5::commit(&bars->pv_done[x]);
+    if (x == last) tc5::commit(&bars->empty_v[s]);
+    return true;
+  };
+  const int n = w.ntiles;
+  bool ok = true;
+  if (n > 0) {
+    ok = mma_s(0, 0);
+    if (ok && w.has_b) ok = mma_s(1, 0);
   }
-  if (ok && w.ntiles > 0) ok = issue_pv(w, smem, bars, tmem, w.ntiles - 1);
+  for (int i = 0; i < n && ok; ++i) {
+    ok = mma_pv(0, i);
+    if (ok && i + 1 < n) ok = mma_s(0, i + 1);
+    if (ok && w.has_b) ok = mma_pv(1, i);
+    if (ok && w.has_b && i + 1 < n) ok = mma_s(1, i + 1);
+  }
   if (!ok) {
     bars->abort = 1;
     report(a.status_flags, kFlagTimeout);
@@ -280,150 +300,73 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Max of the visible scores of a row (keys e < nvis of the tile), eight
-// independent chains.
+// Max of the visible scores (keys e < nvis of the tile) of this thread's row
+// of the S buffer at taddr, read 32 columns at a time; eight independent
+// chains.
 template <bool kMasked>
-__device__ __forceinline__ float row_max(const float (&v)[kN], int nvis) {
+__device__ __forceinline__ float tile_max(uint32_t taddr, int nvis) {
   float m[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < kN; ++e)
-    if (!kMasked || e < nvis) m[e & 7] = fmaxf(m[e & 7], v[e]);
+  for (int c = 0; c < kN / 32; ++c) {
+    float v[32];
+    tc5::tmem_ld32(taddr + c * 32, v);
+    tc5::wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (!kMasked || c * 32 + e < nvis) m[e & 7] = fmaxf(m[e & 7], v[e]);
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], m[j + 4]);
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere), written as
-// bf16 to row r of the swizzled P tile; returns the row's sum of P.
+// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere) as packed
+// bf16 pairs (pk[k/2] holds keys k, k+1); returns the row's sum of P.
 template <bool kMasked>
-__device__ __forceinline__ float write_p(const float (&v)[kN], int nvis, float sl2, float u,
-                                         uint8_t* p_tile, int r) {
+__device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, float u,
+                                          uint32_t (&pk)[kN / 2]) {
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.f;
   const float nu = -u;
 #pragma unroll
-  for (int kc = 0; kc < kN / 8; ++kc) {
-    float p[8];
+  for (int c = 0; c < kN / 32; ++c) {
+    float v[32];
+    tc5::tmem_ld32(taddr + c * 32, v);
+    tc5::wait_ld();
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int k = kc * 8 + e;
-      p[e] = ex2_approx(fmaf(v[k], sl2, nu));
-      if (kMasked) p[e] = (k < nvis) ? p[e] : 0.f;
-      acc[e] += p[e];
+    for (int e = 0; e < 32; e += 2) {
+      const int k = c * 32 + e;
+      float p0 = ex2_approx(fmaf(v[e], sl2, nu));
+      float p1 = ex2_approx(fmaf(v[e + 1], sl2, nu));
+      if (kMasked) {
+        p0 = (k < nvis) ? p0 : 0.f;
+        p1 = (k + 1 < nvis) ? p1 : 0.f;
+      }
+      acc[e & 7] += p0;
+      acc[(e + 1) & 7] += p1;
+      pk[k >> 1] = pack_bf16x2(p0, p1);
     }
-    uint4 pk;
-    pk.x = pack_bf16x2(p[0], p[1]);
-    pk.y = pack_bf16x2(p[2], p[3]);
-    pk.z = pack_bf16x2(p[4], p[5]);
-    pk.w = pack_bf16x2(p[6], p[7]);
-    *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) = pk;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] += acc[j + 4];
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-__device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
-                             uint32_t tmem) {
-  const int r = threadIdx.x;                   // row of the tile = tensor-memory lane
-  const int warp = r >> 5, lane = r & 31;
-  const int rg = w.mt * kM + r;
+// The output rows of tile x: O / l (bf16, or the fp32 partial of the split)
+// and the log-sum-exp.  Kept out of line: the indices are recomputed here
+// instead of living in registers through the softmax loop.
+__device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
+                                        int x, float m_ref, float l) {
+  const int r = threadIdx.x - x * kM;
+  const int rg = w.mt * 2 * kM + x * kM + r;
   const bool valid = rg < w.rows;
   const int t = valid ? rg / a.group : 0;
   const int hh = valid ? rg - t * a.group : 0;
-  // keys [k0, lim) are visible to this row
-  const int lim = valid ? max(w.k0, min(w.k1, w.L - a.q_len + t + 1)) : w.k0;
-  const uint32_t lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  uint8_t* p_tile = smem + kOffP;
-  const float sl2 = a.scale_log2;
-
-  float m_ref = -INFINITY;                     // reference max (log2 units) of P
-  float l = 0.f;                               // sum of P
-  bool ok = true;
-  for (int i = 0; i < w.ntiles; ++i) {
-    const int s = i & 1;
-    if (!warp_wait(&bars->s_full[s], (i >> 1) & 1)) {
-      ok = false;
-      break;
-    }
-    tc5::fence_after_sync();
-    float v[kN];
-#pragma unroll
-    for (int c = 0; c < kN / 32; ++c) tc5::tmem_ld32(lanes + kColS + s * kN + c * 32, v + c * 32);
-    tc5::wait_ld();
-    tc5::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->s_free[s]);
-
-    const int kb = w.k0 + i * kN;
-    const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
-    // interior tiles (every row of the warp sees all 128 keys) skip the masks
-    const bool whole = __all_sync(0xffffffffu, nvis == kN);
-    const float mx = whole ? row_max<false>(v, nvis) : row_max<true>(v, nvis);
-    const float m_tile = mx * sl2;
-    const bool grow = m_tile > m_ref + kRescaleLog2;
-    const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
-    if (grow) m_ref = m_tile;
-
-    // O += P_{i-1} V_{i-1} must have finished before P is rewritten or O rescaled
-    if (i > 0) {
-      if (!warp_wait(&bars->o_done, (i - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc5::fence_after_sync();
-      if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll 1
-        for (int c = 0; c < kHeadDim / 32; ++c) {
-          float o[32];
-          tc5::tmem_ld32(lanes + kColO + c * 32, o);
-          tc5::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc5::tmem_st32(lanes + kColO + c * 32, o);
-        }
-        tc5::wait_st();
-      }
-    }
-    const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
-    l = l * alpha + (whole ? write_p<false>(v, nvis, sl2, u, p_tile, r)
-                           : write_p<true>(v, nvis, sl2, u, p_tile, r));
-    // Tail tile: cache slots past the last visible key may hold anything
-    // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
-    // their V rows are zeroed before the tensor core reads them.
-    if (kb + kN > w.key_end) {
-      if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      if (kb + r >= w.key_end) {
-        uint8_t* vrow = smem + kOffStage + s * kStageBytes + kTile + r * 128;
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = z;
-          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
-        }
-      }
-    }
-    tc5::fence_smem_for_async();
-    tc5::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->p_full);
-  }
-  if (ok && w.ntiles > 0) {
-    ok = warp_wait(&bars->o_done, (w.ntiles - 1) & 1);
-    tc5::fence_after_sync();
-  }
-  if (!ok) {
-    bars->abort = 1;
-    report(a.status_flags, kFlagTimeout);
-    return;
-  }
-
+  const uint32_t o_cols =
+      tmem + (static_cast<uint32_t>((r >> 5) * 32) << 16) + kColO + x * kN;
   const int h = w.g * a.group + hh;
   const long long row = (static_cast<long long>(w.b) * a.q_len + t) * a.num_q_heads + h;
   const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -435,18 +378,18 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     for (int c = 0; c < kHeadDim / 32; ++c) {
       float o[32];
       if (have_o) {
-        tc5::tmem_ld32(lanes + kColO + c * 32, o);
+        tc5::tmem_ld32(o_cols + c * 32, o);
         tc5::wait_ld();
       }
       if (valid) {
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           uint4 pk;
-          const float* x = o + q8 * 8;
-          pk.x = have_o ? pack_bf16x2(x[0] * inv, x[1] * inv) : 0u;
-          pk.y = have_o ? pack_bf16x2(x[2] * inv, x[3] * inv) : 0u;
-          pk.z = have_o ? pack_bf16x2(x[4] * inv, x[5] * inv) : 0u;
-          pk.w = have_o ? pack_bf16x2(x[6] * inv, x[7] * inv) : 0u;
+          const float* y = o + q8 * 8;
+          pk.x = have_o ? pack_bf16x2(y[0] * inv, y[1] * inv) : 0u;
+          pk.y = have_o ? pack_bf16x2(y[2] * inv, y[3] * inv) : 0u;
+          pk.z = have_o ? pack_bf16x2(y[4] * inv, y[5] * inv) : 0u;
+          pk.w = have_o ? pack_bf16x2(y[6] * inv, y[7] * inv) : 0u;
           *reinterpret_cast<uint4*>(orow + c * 32 + q8 * 8) = pk;
         }
       }
@@ -459,15 +402,15 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     for (int c = 0; c < kHeadDim / 32; ++c) {
       float o[32];
       if (have_o) {
-        tc5::tmem_ld32(lanes + kColO + c * 32, o);
+        tc5::tmem_ld32(o_cols + c * 32, o);
         tc5::wait_ld();
       }
       if (valid) {
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float* x = o + q4 * 4;
+          const float* y = o + q4 * 4;
           *reinterpret_cast<float4*>(po + c * 32 + q4 * 4) =
-              have_o ? make_float4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv)
+              have_o ? make_float4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
@@ -476,8 +419,113 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   }
 }
 
+__device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
+                             uint32_t tmem, int x) {
+  const int r = threadIdx.x - x * kM;          // row of tile x = tensor-memory lane
+  const int wq = r >> 5, lane = r & 31;
+  const int rg = w.mt * 2 * kM + x * kM + r;
+  const bool valid = rg < w.rows;
+  const int t = valid ? rg / a.group : 0;
+  // keys [k0, lim) are visible to this row
+  const int lim = valid ? max(w.k0, min(w.k1, w.L - a.q_len + t + 1)) : w.k0;
+  const uint32_t lanes = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t s_cols = lanes + kColS + x * kN;
+  const uint32_t o_cols = lanes + kColO + x * kN;
+  uint8_t* p_tile = smem + kOffP;
+  const float sl2 = a.scale_log2;
+  // the PV whose completion frees the P buffer for this tile's P_x(i):
+  // tile B waits PV_A(i); tile A waits the last PV of tile i - 1
+  uint64_t* p_free = (x == 1) ? &bars->pv_done[0] : &bars->pv_done[w.has_b ? 1 : 0];
+
+  float m_ref = -INFINITY;                     // reference max (log2 units) of P
+  float l = 0.f;                               // sum of P
+  bool ok = true;
+  for (int i = 0; i < w.ntiles; ++i) {
+    if (!warp_wait(&bars->s_full[x], i & 1)) {
+      ok = false;
+      break;
+    }
+    tc5::fence_after_sync();
+    const int kb = w.k0 + i * kN;
+    const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
+    // interior tiles (every row of the warp sees all 128 keys) skip the masks
+    const bool whole = __all_sync(0xffffffffu, nvis == kN);
+    const float mx = whole ? tile_max<false>(s_cols, nvis) : tile_max<true>(s_cols, nvis);
+    const float m_tile = mx * sl2;
+    const bool grow = m_tile > m_ref + kRescaleLog2;
+    const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
+    if (grow) m_ref = m_tile;
+    const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
+    uint32_t pk[kN / 2];
+    const float psum = whole ? tile_exp<false>(s_cols, nvis, sl2, u, pk)
+                             : tile_exp<true>(s_cols, nvis, sl2, u, pk);
+    l = l * alpha + psum;
+
+    // the P buffer is free and O_x holds every earlier tile's PV
+    const int need = (x == 1) ? i : i - 1;     // completion index of p_free to wait for
+    if (need >= 0) {
+      if (!warp_wait(p_free, need & 1)) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+    }
+    if (i > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+      for (int c = 0; c < kHeadDim / 32; ++c) {
+        float o[32];
+        tc5::tmem_ld32(o_cols + c * 32, o);
+        tc5::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+        tc5::tmem_st32(o_cols + c * 32, o);
+      }
+      tc5::wait_st();
+    }
+#pragma unroll
+    for (int kc = 0; kc < kN / 8; ++kc)
+      *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) =
+          make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
+    // Tail tile: cache slots past the last visible key may hold anything
+    // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
+    // their V rows are zeroed (by tile A, before either PV reads them).
+    if (x == 0 && kb + kN > w.key_end) {
+      const int s = i & 1;
+      if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (kb + r >= w.key_end) {
+        uint8_t* vrow = smem + kOffV + s * kTile + r * 128;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = z;
+          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
+        }
+      }
+    }
+    tc5::fence_smem_for_async();
+    tc5::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_full[x]);
+  }
+  if (ok && w.ntiles > 0) {
+    ok = warp_wait(&bars->pv_done[x], (w.ntiles - 1) & 1);
+    tc5::fence_after_sync();
+  }
+  if (!ok) {
+    bars->abort = 1;
+    report(a.status_flags, kFlagTimeout);
+    return;
+  }
+  write_rows(a, w, tmem, x, m_ref, l);
+}
+
 // ------------------------------------------------------------------ kernel
 
+// 10 warps: two of the SM's four sub-partitions hold three of them, so a
+// thread gets at most 168 registers (16,384 per sub-partition).
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -496,12 +544,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(&bars->empty_k[s], 1);
       mbar_init(&bars->empty_v[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 4);
+      mbar_init(&bars->pv_done[x], 1);
     }
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     issued = 0;
@@ -513,20 +560,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   // the lengths may come from the previous kernel in the stream
   pdl_wait();
   const Work w = decode_work(a);
-  if (warp < 4) {
-    // Q tile: row r = (token, q head of the group), two swizzled 64-dim halves
-    const int r = threadIdx.x;
-    const int rg = w.mt * kM + r;
+  if (warp < 8) {
+    // Q tiles: thread i loads row i % 128 of tile i / 128 (row = (token, q head
+    // of the group)), two swizzled 64-dim halves
+    const int x = threadIdx.x / kM, r = threadIdx.x % kM;
+    const int rg = w.mt * 2 * kM + threadIdx.x;
     const bool valid = rg < w.rows;
     const int t = valid ? rg / a.group : 0;
     const int hh = valid ? rg - t * a.group : 0;
     const uint4* src = reinterpret_cast<const uint4*>(
         a.q + (static_cast<long long>(w.b) * a.q_len + t) * a.q_stride_t +
         static_cast<long long>(w.g * a.group + hh) * a.q_stride_h);
+    uint8_t* qt = smem + kOffQ + x * kTile;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 x = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(smem + kOffQ + (c >> 3) * kHalf + swz128(r, c & 7)) = x;
+      const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(qt + (c >> 3) * kHalf + swz128(r, c & 7)) = v;
     }
     tc5::fence_smem_for_async();
   }
@@ -537,7 +586,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < 4) {
-    softmax_rows(a, w, smem, bars, tmem);
+    softmax_rows(a, w, smem, bars, tmem, 0);
+  } else if (warp < 8) {
+    if (w.has_b) softmax_rows(a, w, smem, bars, tmem, 1);
   } else if (warp == kProducerWarp) {
     int n = 0;
     produce(a, w, &kmap, &vmap, smem, bars, &n);

@@ -9,6 +9,9 @@
 
 namespace pkvqk {
 
+// Packed (token, q head) rows of one kv head that one CTA covers.
+constexpr int kPrefillRowsPerCta = 256;
+
 struct PrefillArgs {
   const __nv_bfloat16* q;          // [B, q_len, Hq, 128] (strided tokens / heads)
   int64_t q_stride_t, q_stride_h;
@@ -20,7 +23,7 @@ struct PrefillArgs {
   int64_t num_blocks;
   int32_t num_splits;              // >= 1
   int32_t chunk_pages;             // pages per split
-  int32_t m_tiles;                 // ceil(q_len * group / 128)
+  int32_t m_tiles;                 // ceil(q_len * group / kPrefillRowsPerCta)
   float scale_log2;                // softmax scale * log2(e)
   __nv_bfloat16* out;              // num_splits == 1: [B, q_len, Hq, 128]
   float* lse_out;                  // num_splits == 1: optional [B, q_len, Hq]
