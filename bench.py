@@ -515,7 +515,7 @@ def main():
         line["unit"] = "TFLOP/s"
         line["e2e"]["value"] = round(world * flops / (e2e_ms * 1e-3) / 1e12, 2)
         line["e2e"]["unit"] = "TFLOP/s"
-        line["config"]["schedule"] = f"row tiles of 128 x split {S}"
+        line["config"]["schedule"] = f"256-row CTA tiles (2 x 128, ping-pong) x split {S}"
         line["config"]["flops_per_step"] = flops
         line["config"]["kv_bytes_per_step"] = decode_bytes
         del line["pct_of_nominal_8tbs"]

@@ -19,25 +19,29 @@
 // the other tile's MMAs do (ping-pong).  Warp roles:
 //   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (tensor-memory
 //              lane r).  Reads its score row S = Q K^T from tensor memory,
-//              keeps the running max and sum, writes P (bf16) to the shared P
-//              buffer when it is free, rescales O in tensor memory only when
-//              the max grew by more than 2^8 (P <= 2^8 otherwise), and writes
-//              the output row at the end;
+//              keeps the running max and sum, writes P (bf16 pairs) back into
+//              the first 64 columns of its own S buffer, rescales O in tensor
+//              memory only when the max grew by more than 2^8 (P <= 2^8
+//              otherwise), and writes the output row at the end;
 //   warp 8     TMA producer: one box per (page, 64-dim half) of K and of V;
 //   warp 9     allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
-//              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims),
-//              O_x += P_x V_i   (M 128 rows, N 128 dims, K 128 keys).
-// The single P buffer passes A -> B -> A: softmax B writes P_B(i) once
-// PV_A(i) finished, softmax A writes P_A(i+1) once PV_B(i) finished.
+//              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
+//                               operands in shared memory),
+//              O_x += P_x V_i   (M 128 rows, N 128 dims, K 128 keys; P from
+//                               tensor memory, V from shared memory).
+// S_x(i+1) overwrites the columns that held P_x(i): the MMAs of one thread
+// run in issue order, and PV_x(i) is issued first.  The commit that signals
+// S_x(i+1) also covers PV_x(i), so softmax x may rescale O_x as soon as it
+// sees S_x(i+1).
 //
 // Shared memory (1024-byte aligned, 128-byte swizzle everywhere, the layout
 // the MMA descriptors describe):
 //   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]      2 x 32 KiB
-//   P         [2 key halves][128 rows][64 bf16]      32 KiB
 //   K stage s [2 dim halves][128 keys][64 bf16]      2 x 32 KiB
 //   V stage s  the same                              2 x 32 KiB
-// Tensor memory: S_A at columns 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
+// Tensor memory: S_A (then P_A) at columns 0-127, S_B (P_B) 128-255, O_A
+// 256-383, O_B 384-511.
 //
 // Every wait is bounded: on a timeout the CTA reports PKVQK_FLAG_WAIT_TIMEOUT,
 // lets its own copies and MMAs in flight finish (bounded), frees its tensor
@@ -57,8 +61,7 @@ constexpr int kHalf = 128 * 128;               // [128 rows][64 bf16] sub-tile, 
 constexpr int kTile = 2 * kHalf;               // [128 rows][128 bf16], bytes
 constexpr int kStages = 2;
 constexpr int kOffQ = 0;                       // Q_A, Q_B
-constexpr int kOffP = 2 * kTile;
-constexpr int kOffK = 3 * kTile;
+constexpr int kOffK = 2 * kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kDataBytes = kOffV + kStages * kTile;
 constexpr int kThreads = 10 * 32;
@@ -73,9 +76,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct Bars {
   uint64_t full_k[kStages], full_v[kStages];     // TMA landed
   uint64_t empty_k[kStages], empty_v[kStages];   // the MMAs reading a stage finished
-  uint64_t s_full[2];                            // S_x written
+  uint64_t s_full[2];                            // S_x written (and the PV before it done)
   uint64_t p_full[2];                            // P_x written (and O_x rescaled)
-  uint64_t pv_done[2];                           // O_x += P_x V finished
+  uint64_t pv_done[2];                           // the last O_x += P_x V finished
   uint64_t drain;                                // MMA thread's own completion (timeout path)
   uint32_t tmem_base;
   int32_t abort;
@@ -237,7 +240,7 @@ __device__ void drain_copies(Bars* bars, int issued) {
 __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
                            uint32_t tmem) {
   const int last = w.has_b ? 1 : 0;            // the row tile that reads a stage last
-  const uint32_t p = smem_addr(smem + kOffP);
+  const int n = w.ntiles;
   constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(kM, kN, false);
   constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kM, kHeadDim, true);
   // S_x(i) = Q_x K_i^T
@@ -262,15 +265,15 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     if (x == 0 && !mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
     const uint32_t vt = smem_addr(smem + kOffV + s * kTile);
+    // P_x: 16 keys per step = 8 columns of bf16 pairs
 #pragma unroll
     for (int ks = 0; ks < kN / 16; ++ks)
-      tc5::mma_f16(tmem + kColO + x * kN, desc_k_major(p, ks), desc_v(vt, ks), idesc_pv,
-                   (i > 0 || ks > 0) ? 1u : 0u);
-    tc5::commit(&bars->pv_done[x]);
+      tc5::mma_f16_ts(tmem + kColO + x * kN, tmem + kColS + x * kN + ks * 8, desc_v(vt, ks),
+                      idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+    if (i == n - 1) tc5::commit(&bars->pv_done[x]);
     if (x == last) tc5::commit(&bars->empty_v[s]);
     return true;
   };
-  const int n = w.ntiles;
   bool ok = true;
   if (n > 0) {
     ok = mma_s(0, 0);
@@ -300,37 +303,40 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Max of the visible scores (keys e < nvis of the tile) of this thread's row
-// of the S buffer at taddr, read 32 columns at a time; eight independent
-// chains.
-template <bool kMasked>
-__device__ __forceinline__ float tile_max(uint32_t taddr, int nvis) {
-  float m[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < kN / 32; ++c) {
-    float v[32];
-    tc5::tmem_ld32(taddr + c * 32, v);
-    tc5::wait_ld();
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (!kMasked || c * 32 + e < nvis) m[e & 7] = fmaxf(m[e & 7], v[e]);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], m[j + 4]);
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere) as packed
-// bf16 pairs (pk[k/2] holds keys k, k+1); returns the row's sum of P.
+// Two fp32 values in one 64-bit register pair, and the packed f32x2 add/fma.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Max of the visible scores (keys e < nvis of the tile) of this thread's row
+// of the S buffer at taddr, read 32 columns at a time; four independent
+// three-input chains.
 template <bool kMasked>
-__device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, float u,
-                                          uint32_t (&pk)[kN / 2]) {
-  float acc[8];
+__device__ __forceinline__ float tile_max(uint32_t taddr, int nvis) {
+  float m[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  const float nu = -u;
+  for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
 #pragma unroll
   for (int c = 0; c < kN / 32; ++c) {
     float v[32];
@@ -338,21 +344,52 @@ __device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, f
     tc5::wait_ld();
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      const int k = c * 32 + e;
-      float p0 = ex2_approx(fmaf(v[e], sl2, nu));
-      float p1 = ex2_approx(fmaf(v[e + 1], sl2, nu));
+      float a0 = v[e], a1 = v[e + 1];
+      if (kMasked) {
+        a0 = (c * 32 + e < nvis) ? a0 : -INFINITY;
+        a1 = (c * 32 + e + 1 < nvis) ? a1 : -INFINITY;
+      }
+      m[(e >> 1) & 3] = max3(m[(e >> 1) & 3], a0, a1);
+    }
+  }
+  return max3(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
+// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere), rounded to
+// bf16 and written back as pairs (keys k, k+1 in column k/2) over the first
+// 64 columns of the same S buffer, each chunk after it has been read.
+// Returns the row's sum of P (before rounding).
+template <bool kMasked>
+__device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, float u) {
+  const uint64_t scale2 = pack2(sl2, sl2), shift2 = pack2(-u, -u);
+  uint64_t acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = pack2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < kN / 32; ++c) {
+    float v[32];
+    tc5::tmem_ld32(taddr + c * 32, v);
+    tc5::wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int k = c * 32 + 2 * q;
+      float x0, x1;
+      unpack2(fma2(pack2(v[2 * q], v[2 * q + 1]), scale2, shift2), x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
       if (kMasked) {
         p0 = (k < nvis) ? p0 : 0.f;
         p1 = (k + 1 < nvis) ? p1 : 0.f;
       }
-      acc[e & 7] += p0;
-      acc[(e + 1) & 7] += p1;
-      pk[k >> 1] = pack_bf16x2(p0, p1);
+      acc[q & 3] = add2(acc[q & 3], pack2(p0, p1));
+      pk[q] = pack_bf16x2(p0, p1);
     }
+    tc5::tmem_st16(taddr + c * 16, pk);
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] += acc[j + 4];
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  const uint64_t t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  float t0, t1;
+  unpack2(t, t0, t1);
+  return t0 + t1;
 }
 
 // The output rows of tile x: O / l (bf16, or the fp32 partial of the split)
@@ -431,16 +468,13 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   const uint32_t lanes = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t s_cols = lanes + kColS + x * kN;
   const uint32_t o_cols = lanes + kColO + x * kN;
-  uint8_t* p_tile = smem + kOffP;
   const float sl2 = a.scale_log2;
-  // the PV whose completion frees the P buffer for this tile's P_x(i):
-  // tile B waits PV_A(i); tile A waits the last PV of tile i - 1
-  uint64_t* p_free = (x == 1) ? &bars->pv_done[0] : &bars->pv_done[w.has_b ? 1 : 0];
 
   float m_ref = -INFINITY;                     // reference max (log2 units) of P
   float l = 0.f;                               // sum of P
   bool ok = true;
   for (int i = 0; i < w.ntiles; ++i) {
+    // S_x(i) landed, and with it PV_x(i - 1): O_x is complete up to tile i - 1
     if (!warp_wait(&bars->s_full[x], i & 1)) {
       ok = false;
       break;
@@ -456,20 +490,6 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
     if (grow) m_ref = m_tile;
     const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
-    uint32_t pk[kN / 2];
-    const float psum = whole ? tile_exp<false>(s_cols, nvis, sl2, u, pk)
-                             : tile_exp<true>(s_cols, nvis, sl2, u, pk);
-    l = l * alpha + psum;
-
-    // the P buffer is free and O_x holds every earlier tile's PV
-    const int need = (x == 1) ? i : i - 1;     // completion index of p_free to wait for
-    if (need >= 0) {
-      if (!warp_wait(p_free, need & 1)) {
-        ok = false;
-        break;
-      }
-      tc5::fence_after_sync();
-    }
     if (i > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
       for (int c = 0; c < kHeadDim / 32; ++c) {
@@ -480,12 +500,10 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
         for (int e = 0; e < 32; ++e) o[e] *= alpha;
         tc5::tmem_st32(o_cols + c * 32, o);
       }
-      tc5::wait_st();
     }
-#pragma unroll
-    for (int kc = 0; kc < kN / 8; ++kc)
-      *reinterpret_cast<uint4*>(p_tile + (kc >> 3) * kHalf + swz128(r, kc & 7)) =
-          make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
+    const float psum = whole ? tile_exp<false>(s_cols, nvis, sl2, u)
+                             : tile_exp<true>(s_cols, nvis, sl2, u);
+    l = l * alpha + psum;
     // Tail tile: cache slots past the last visible key may hold anything
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
     // their V rows are zeroed (by tile A, before either PV reads them).
@@ -504,14 +522,15 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
           *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
         }
       }
+      tc5::fence_smem_for_async();
     }
-    tc5::fence_smem_for_async();
+    tc5::wait_st();
     tc5::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->p_full[x]);
   }
   if (ok && w.ntiles > 0) {
-    ok = warp_wait(&bars->pv_done[x], (w.ntiles - 1) & 1);
+    ok = warp_wait(&bars->pv_done[x], 0);
     tc5::fence_after_sync();
   }
   if (!ok) {
