@@ -63,6 +63,9 @@ PREFILL_WORKLOADS = {
     "prefill_gqa8_8x512": ("chunked_prefill", {"Hq": 32, "Hkv": 4},
                            "chunked prefill 32q/4kv D128 bs16, batch 8 x 512-token chunk, "
                            "prior context U[0, 6144]"),
+    "prefill_varlen_16": ("varlen_prefill", {},
+                          "varlen prefill 16q/8kv D128 bs16, 16 fresh prompts of U[128, 2048] "
+                          "tokens, packed"),
     "verify_32x5_tc": ("verify_causal", {},
                        "speculative verify 16q/8kv D128 bs16, batch 32, 5 query tokens, prior "
                        "U[2048,8192], on the tensor-core multi-query kernel"),
@@ -108,10 +111,10 @@ def load_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
 def attention_flops(p):
     """Algorithmic FLOPs of the causal attention: per visible (query token,
     key) pair and q head, 2*D for q.k and 2*D for p*v."""
-    T = p.q_len
+    q_lens = p.q_lens_host if p.q_lens_host is not None else [p.q_len] * p.B
     n = 0
-    for L in p.seq_lens_host:
-        L = int(L)
+    for L, T in zip(p.seq_lens_host, q_lens):
+        L, T = int(L), int(T)
         # token t sees L - T + t + 1 keys (clipped at 0)
         n += sum(max(0, L - T + t + 1) for t in range(T))
     return 4 * p.D * p.Hq * n
@@ -325,21 +328,27 @@ def main():
     if prefill:
         S = args.num_splits if args.num_splits >= 1 else lib.choose_prefill_splits(
             p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
-        ws_bytes = lib.prefill_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+        ws_bytes = lib.prefill_workspace_bytes(1, p.T, p.Hq, p.D, S)
     else:
         S = args.num_splits if args.num_splits >= 0 else lib.choose_num_splits(
             p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
         ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if ws_bytes else None
-    out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev)
+    varlen = p.cu_seqlens is not None
+    out = (torch.empty(p.T, p.Hq, p.D, dtype=torch.bfloat16, device=dev) if varlen else
+           torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev))
     q = p.q.clone()
     stream = torch.cuda.current_stream()
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     big_inputs = decode_bytes > 4 * l2_bytes
     flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
 
-    def decode_call(qq, bt, sl):
-        if prefill:
+    def decode_call(qq, bt, sl, cu=None):
+        if varlen:
+            lib.paged_prefill_varlen(qq, p.cu_seqlens if cu is None else cu, p.q_len,
+                                     p.k_cache, p.v_cache, bt, sl, out, num_splits=S,
+                                     max_seq_len_hint=p.max_seq_len, workspace=ws, stream=stream)
+        elif prefill:
             lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len,
                               num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
                               stream=stream)
@@ -404,6 +413,8 @@ def main():
     # the step's inputs packed into one pinned host buffer (16-byte aligned
     # fields), one host->device copy, typed device views into the copy
     names = ("q", "k", "v", "positions", "slot_mapping", "block_tables", "seq_lens")
+    if varlen:
+        names = names + ("cu_seqlens",)
     fields, off = {}, 0
     for n in names:
         t = getattr(p, n)
@@ -427,7 +438,8 @@ def main():
         lib.norm_rope_append(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["positions"],
                              dev_in["slot_mapping"], p.gamma_q, p.gamma_k, p.theta, p.eps,
                              p.k_cache, p.v_cache, stream=stream)
-        decode_call(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"])
+        decode_call(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"],
+                    dev_in.get("cu_seqlens"))
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

@@ -16,7 +16,9 @@
  *      split partials.
  *   4. pkvqk_paged_prefill    — item 4 (chunked prefill): the same causal
  *      attention for many new tokens per sequence (a prefill chunk after
- *      its prior context), on the tensor cores.
+ *      its prior context), on the tensor cores; pkvqk_paged_prefill_varlen
+ *      takes a different number of new tokens per sequence (item 1's
+ *      varlen prefill).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -341,6 +343,42 @@ PKVQK_API pkvqk_status pkvqk_paged_prefill(
     const int32_t* block_tables, int32_t max_blocks_per_seq,
     const int32_t* seq_lens,
     int32_t batch, int32_t q_len, int32_t num_q_heads,
+    int32_t num_splits, int32_t max_seq_len_hint, float scale,
+    void* out, float* lse_out,
+    void* workspace, size_t workspace_bytes,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/*
+ * Varlen form of pkvqk_paged_prefill: every sequence brings its own number of
+ * new tokens, packed back to back (the FlashAttention-2 varlen convention the
+ * pages use for prefill, Summary item 1).  Source: InfiniLM PR #585, "概述 /
+ * Summary" items 1 (varlen prefill, paged cache) and 4 (chunked prefill).
+ *
+ * Sequence b's q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens are
+ * rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q, out and lse_out; token t
+ * of it sees the keys n < seq_lens[b] - q_len_b + t + 1 (seq_lens counting the
+ * new tokens).  A fresh prompt has seq_lens[b] == q_len_b; a later chunk of a
+ * prompt, or a verify step, has more keys than new tokens.
+ *
+ *   q              device bf16, row i at q[i*q_stride_t + h*q_stride_h + d]
+ *   cu_seqlens_q   device int32 [batch + 1], non-decreasing, cu_seqlens_q[0] = 0
+ *   max_q_len      host int >= every q_len_b (1..16384): sizes the grid (no
+ *                  device read); tokens past it are not computed
+ *   total_q        host: rows of q / out / lse_out (= cu_seqlens_q[batch]);
+ *                  rows at or past it are never written
+ *   out            device bf16 [total_q, Hq, head_dim], contiguous
+ *   lse_out        device fp32 [total_q, Hq] or NULL
+ *   workspace      num_splits > 1: >= pkvqk_prefill_workspace_bytes(1, total_q,
+ *                  Hq, head_dim, num_splits)
+ * Everything else as pkvqk_paged_prefill.
+ */
+PKVQK_API pkvqk_status pkvqk_paged_prefill_varlen(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const int32_t* cu_seqlens_q, int32_t max_q_len, int64_t total_q,
+    const void* k_cache, const void* v_cache, const pkvqk_cache_layout* layout,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens,
+    int32_t batch, int32_t num_q_heads,
     int32_t num_splits, int32_t max_seq_len_hint, float scale,
     void* out, float* lse_out,
     void* workspace, size_t workspace_bytes,

@@ -100,13 +100,21 @@ pkvqk_prefill_workspace_bytes = _sig("pkvqk_prefill_workspace_bytes", c_size,
                                      [c_i32, c_i32, c_i32, c_i32, c_i32])
 pkvqk_paged_prefill = _sig("pkvqk_paged_prefill", ctypes.c_int,
                            _decode_args + [c_vp, c_vp, c_vp, c_size, c_vp, c_vp])
+pkvqk_paged_prefill_varlen = _sig("pkvqk_paged_prefill_varlen", ctypes.c_int, [
+    c_vp, c_i64, c_i64,                 # q, strides
+    c_vp, c_i32, c_i64,                 # cu_seqlens_q, max_q_len, total_q
+    c_vp, c_vp, ctypes.POINTER(CacheLayout),
+    c_vp, c_i32, c_vp,                  # block_tables, max_blocks_per_seq, seq_lens
+    c_i32, c_i32,                       # batch, num_q_heads
+    c_i32, c_i32, c_f32,                # num_splits, max_seq_len_hint, scale
+    c_vp, c_vp, c_vp, c_size, c_vp, c_vp])
 
 EXPORTED = [
     "pkvqk_last_error", "pkvqk_abi_version", "pkvqk_norm_rope_append",
     "pkvqk_choose_num_splits", "pkvqk_decode_workspace_bytes", "pkvqk_paged_decode",
     "pkvqk_paged_decode_partials", "pkvqk_lse_combine", "pkvqk_paged_decode_static_ws",
     "pkvqk_static_workspace_capacity", "pkvqk_choose_prefill_splits",
-    "pkvqk_prefill_workspace_bytes", "pkvqk_paged_prefill",
+    "pkvqk_prefill_workspace_bytes", "pkvqk_paged_prefill", "pkvqk_paged_prefill_varlen",
 ]
 
 
@@ -246,5 +254,30 @@ def paged_prefill(q, k_cache, v_cache, block_tables, seq_lens, out, *, q_len, nu
         _ptr(k_cache), _ptr(v_cache), ctypes.byref(lay),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
         B, q_len, Hq, int(num_splits), int(max_seq_len_hint), float(scale),
+        _ptr(out), _ptr(lse_out), _ptr(workspace), ws_bytes,
+        _ptr(status_flags), _stream(stream)))
+
+
+def paged_prefill_varlen(q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables, seq_lens,
+                         out, *, num_splits=1, max_seq_len_hint=0, scale=0.0, lse_out=None,
+                         workspace=None, status_flags=None, stream=None):
+    """Varlen causal multi-query attention on the tensor cores.
+
+    q [total_q, Hq, D] packed rows, cu_seqlens_q int32 [B + 1] on the device,
+    max_q_len a host int; out [total_q, Hq, D] contiguous bf16.
+    """
+    total_q, Hq, D = q.shape
+    B = cu_seqlens_q.shape[0] - 1
+    lay = cache_layout(k_cache)
+    if tuple(v_cache.stride()) != tuple(k_cache.stride()) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must share one layout")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(pkvqk_paged_prefill_varlen(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(cu_seqlens_q), int(max_q_len), int(total_q),
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(lay),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        B, Hq, int(num_splits), int(max_seq_len_hint), float(scale),
         _ptr(out), _ptr(lse_out), _ptr(workspace), ws_bytes,
         _ptr(status_flags), _stream(stream)))

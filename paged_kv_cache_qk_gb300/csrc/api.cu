@@ -321,12 +321,17 @@ size_t prefill_bytes(int64_t rows, int S) {
   return (raw + 255) & ~size_t(255);
 }
 
-pkvqk_status run_prefill(const DecodeCall& c) {
+// cu_seqlens_q == nullptr: every sequence has c.q_len new tokens (total_q is
+// then batch * q_len); else varlen with c.q_len the longest.
+pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64_t total_q) {
   PKVQK_TRY(check_layout(c.layout));
   const pkvqk_cache_layout& L = *c.layout;
   if (c.batch < 0 || c.batch > 65535) return fail(PKVQK_ERR_INVALID_ARG, "batch %d", c.batch);
   if (c.q_len < 1 || c.q_len > 16384)
-    return fail(PKVQK_ERR_INVALID_ARG, "q_len %d (1..16384)", c.q_len);
+    return fail(PKVQK_ERR_INVALID_ARG, "%s %d (1..16384)",
+                cu_seqlens_q != nullptr ? "max_q_len" : "q_len", c.q_len);
+  if (total_q < 0 || total_q > INT32_MAX)
+    return fail(PKVQK_ERR_INVALID_ARG, "total_q %lld (0..2^31-1)", static_cast<long long>(total_q));
   if (c.num_q_heads < 1 || (c.num_q_heads % L.num_kv_heads) != 0)
     return fail(PKVQK_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
                 c.num_q_heads, L.num_kv_heads);
@@ -351,18 +356,21 @@ pkvqk_status run_prefill(const DecodeCall& c) {
   const int64_t grid_x = static_cast<int64_t>(m_tiles) * L.num_kv_heads * S;
   if (grid_x > INT32_MAX) return fail(PKVQK_ERR_UNSUPPORTED, "too many CTAs (%lld)",
                                       static_cast<long long>(grid_x));
-  const int64_t nrows = static_cast<int64_t>(c.batch) * c.q_len * c.num_q_heads;
+  const int64_t nrows = total_q * c.num_q_heads;
+  if (nrows > INT32_MAX)
+    return fail(PKVQK_ERR_UNSUPPORTED, "total_q * num_q_heads exceeds 2^31 - 1");
   const size_t need = prefill_bytes(nrows, S);
   if (need > 0 && c.workspace_bytes < need)
     return fail(PKVQK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed",
                 c.workspace_bytes, need);
-  if (c.batch == 0) return ok();
+  if (c.batch == 0 || total_q == 0) return ok();
 
   PKVQK_TRY(check_device_ptr(c.q, "q"));
   PKVQK_TRY(check_device_ptr(c.k_cache, "k_cache"));
   PKVQK_TRY(check_device_ptr(c.v_cache, "v_cache"));
   PKVQK_TRY(check_device_ptr(c.block_tables, "block_tables"));
   PKVQK_TRY(check_device_ptr(c.seq_lens, "seq_lens"));
+  if (cu_seqlens_q != nullptr) PKVQK_TRY(check_device_ptr(cu_seqlens_q, "cu_seqlens_q"));
   PKVQK_TRY(check_device_ptr(c.out, "out"));
   if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
   if (!aligned16(c.q) || !aligned16(c.out))
@@ -396,6 +404,8 @@ pkvqk_status run_prefill(const DecodeCall& c) {
   a.num_q_heads = c.num_q_heads;
   a.num_kv_heads = L.num_kv_heads;
   a.group = group;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.total_q = total_q;
   a.block_size = L.block_size;
   a.num_blocks = L.num_blocks;
   a.num_splits = S;
@@ -641,7 +651,26 @@ pkvqk_status pkvqk_paged_prefill(const void* q, int64_t q_stride_t, int64_t q_st
                q_len,      num_q_heads, num_splits,       max_seq_len_hint, scale,
                out,        lse_out,     workspace,        workspace_bytes_, status_flags,
                reinterpret_cast<cudaStream_t>(stream), false};
-  return run_prefill(c);
+  return run_prefill(c, nullptr, static_cast<int64_t>(batch) * q_len);
+}
+
+pkvqk_status pkvqk_paged_prefill_varlen(const void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                        const int32_t* cu_seqlens_q, int32_t max_q_len,
+                                        int64_t total_q, const void* k_cache,
+                                        const void* v_cache, const pkvqk_cache_layout* layout,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        int32_t num_q_heads, int32_t num_splits,
+                                        int32_t max_seq_len_hint, float scale, void* out,
+                                        float* lse_out, void* workspace, size_t workspace_bytes_,
+                                        int32_t* status_flags, pkvqk_stream_t stream) {
+  if (cu_seqlens_q == nullptr) return fail(PKVQK_ERR_INVALID_ARG, "cu_seqlens_q is NULL");
+  DecodeCall c{q,          q_stride_t,  q_stride_h,       k_cache,    v_cache,
+               layout,     block_tables, max_blocks_per_seq, seq_lens, batch,
+               max_q_len,  num_q_heads, num_splits,       max_seq_len_hint, scale,
+               out,        lse_out,     workspace,        workspace_bytes_, status_flags,
+               reinterpret_cast<cudaStream_t>(stream), false};
+  return run_prefill(c, cu_seqlens_q, total_q);
 }
 
 }  // extern "C"

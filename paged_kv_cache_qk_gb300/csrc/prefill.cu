@@ -9,7 +9,10 @@
 // b (t < q_len) sits at position seq_len - q_len + t and attends to the keys
 // n <= seq_len - q_len + t of its own sequence, gathered page by page through
 // the block table; q head h reads kv head h / group; softmax scale D^-1/2
-// unless the caller gives one.
+// unless the caller gives one.  q_len is either one value for the batch or,
+// varlen (the FlashAttention-2 varlen role of Summary item 1), per sequence
+// from cumulative row offsets; the grid covers the longest, and row tiles past
+// a shorter sequence's rows do nothing.
 //
 // One CTA = two tiles A and B of 128 packed rows r = t * group + (h % group)
 // of one (sequence, kv head) -- 256 consecutive rows -- restricted to one
@@ -128,6 +131,8 @@ struct Work {
   int k0, k1;    // the split's key range
   int key_end;   // keys at or past key_end are visible to no row of the CTA
   int ntiles;
+  int q_len;     // this sequence's new tokens
+  long long q0;  // row of q/out holding its token 0
   int rows;      // q_len * group
   bool has_b;    // row tile B holds rows
 };
@@ -146,13 +151,21 @@ __device__ Work decode_work(const PrefillArgs& a) {
   const long long chunk_keys = static_cast<long long>(a.chunk_pages) * a.block_size;
   w.k0 = static_cast<int>(min(L, w.j * chunk_keys));
   w.k1 = (w.j == a.num_splits - 1) ? w.L : static_cast<int>(min(L, (w.j + 1) * chunk_keys));
-  w.rows = a.q_len * a.group;
+  if (a.cu_seqlens_q != nullptr) {
+    const long long c0 = a.cu_seqlens_q[w.b], c1 = a.cu_seqlens_q[w.b + 1];
+    w.q0 = c0;
+    w.q_len = static_cast<int>(max(0ll, min(c1 - c0, static_cast<long long>(a.q_len))));
+  } else {
+    w.q0 = static_cast<long long>(w.b) * a.q_len;
+    w.q_len = a.q_len;
+  }
+  w.rows = w.q_len * a.group;
   const int row0 = w.mt * 2 * kM;
   w.has_b = row0 + kM < w.rows;
   const int last_row = min(row0 + 2 * kM - 1, w.rows - 1);
   const int t_last = last_row / a.group;
-  w.key_end = max(w.k0, min(w.k1, w.L - a.q_len + t_last + 1));
-  w.ntiles = (w.key_end - w.k0 + kN - 1) / kN;
+  w.key_end = max(w.k0, min(w.k1, w.L - w.q_len + t_last + 1));
+  w.ntiles = row0 < w.rows ? (w.key_end - w.k0 + kN - 1) / kN : 0;
   return w;
 }
 
@@ -399,13 +412,16 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
                                         int x, float m_ref, float l) {
   const int r = threadIdx.x - x * kM;
   const int rg = w.mt * 2 * kM + x * kM + r;
-  const bool valid = rg < w.rows;
-  const int t = valid ? rg / a.group : 0;
+  const int t0 = rg / a.group;
+  // rows outside the sequence, or (inconsistent offsets) outside q/out: no write;
+  // every lane still takes part in the warp-wide tensor-memory loads below
+  const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
+  const int t = valid ? t0 : 0;
   const int hh = valid ? rg - t * a.group : 0;
   const uint32_t o_cols =
       tmem + (static_cast<uint32_t>((r >> 5) * 32) << 16) + kColO + x * kN;
   const int h = w.g * a.group + hh;
-  const long long row = (static_cast<long long>(w.b) * a.q_len + t) * a.num_q_heads + h;
+  const long long row = (w.q0 + t) * a.num_q_heads + h;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   const bool have_o = w.ntiles > 0;            // uniform over the CTA
@@ -464,7 +480,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   const bool valid = rg < w.rows;
   const int t = valid ? rg / a.group : 0;
   // keys [k0, lim) are visible to this row
-  const int lim = valid ? max(w.k0, min(w.k1, w.L - a.q_len + t + 1)) : w.k0;
+  const int lim = valid ? max(w.k0, min(w.k1, w.L - w.q_len + t + 1)) : w.k0;
   const uint32_t lanes = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t s_cols = lanes + kColS + x * kN;
   const uint32_t o_cols = lanes + kColO + x * kN;
@@ -584,11 +600,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     // of the group)), two swizzled 64-dim halves
     const int x = threadIdx.x / kM, r = threadIdx.x % kM;
     const int rg = w.mt * 2 * kM + threadIdx.x;
-    const bool valid = rg < w.rows;
-    const int t = valid ? rg / a.group : 0;
+    const int t0 = rg / a.group;
+    const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
+    const int t = valid ? t0 : 0;
     const int hh = valid ? rg - t * a.group : 0;
     const uint4* src = reinterpret_cast<const uint4*>(
-        a.q + (static_cast<long long>(w.b) * a.q_len + t) * a.q_stride_t +
+        a.q + (valid ? w.q0 + t : 0) * a.q_stride_t +
         static_cast<long long>(w.g * a.group + hh) * a.q_stride_h);
     uint8_t* qt = smem + kOffQ + x * kTile;
 #pragma unroll

@@ -13,20 +13,25 @@ namespace pkvqk {
 constexpr int kPrefillRowsPerCta = 256;
 
 struct PrefillArgs {
-  const __nv_bfloat16* q;          // [B, q_len, Hq, 128] (strided tokens / heads)
+  const __nv_bfloat16* q;          // [tokens, Hq, 128] (strided tokens / heads)
   int64_t q_stride_t, q_stride_h;
   const int32_t* block_tables;     // [B, max_blocks_per_seq]
   int32_t max_blocks_per_seq;
   const int32_t* seq_lens;         // [B], counting the q_len new tokens
   int32_t batch, q_len, num_q_heads, num_kv_heads, group;
+  // varlen: sequence b's new tokens are rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+  // of q/out (q_len is then their maximum); NULL: every sequence has q_len, at
+  // rows b * q_len ..
+  const int32_t* cu_seqlens_q;
+  int64_t total_q;                 // rows of q/out (rows past it are never written)
   int32_t block_size;
   int64_t num_blocks;
   int32_t num_splits;              // >= 1
   int32_t chunk_pages;             // pages per split
   int32_t m_tiles;                 // ceil(q_len * group / kPrefillRowsPerCta)
   float scale_log2;                // softmax scale * log2(e)
-  __nv_bfloat16* out;              // num_splits == 1: [B, q_len, Hq, 128]
-  float* lse_out;                  // num_splits == 1: optional [B, q_len, Hq]
+  __nv_bfloat16* out;              // num_splits == 1: [tokens, Hq, 128]
+  float* lse_out;                  // num_splits == 1: optional [tokens, Hq]
   float* ws_o;                     // num_splits > 1: [rows, S, 128] normalised partials
   float* ws_lse;                   // num_splits > 1: [rows, S]
   int32_t* status_flags;

@@ -18,6 +18,8 @@ PR #585, Qwen3-0.6B / 1.7B; InfiniLM issue #498, Qwen3-30B-A3B with
                         pages needed, shuffled block ids.
 * ``verify_causal``     16q/8kv, D=128, batch 32, 5 query tokens per sequence
                         (k = 4 draft tokens + 1), prior context U[2048, 8192].
+* ``varlen_prefill``    16q/8kv, D=128, batch 16 fresh prompts of U[128, 2048]
+                        tokens each, packed back to back (varlen).
 * ``chunked_prefill``   16q/8kv, D=128, batch 8, a chunk of 512 new tokens per
                         sequence after a prior context U[0, 6144] (the chunks
                         of a ~6.5k-token prompt, the size the pages inject in
@@ -66,6 +68,9 @@ class Problem:
     v_cache: torch.Tensor              # bf16 [NB, bs, Hkv, D]
     block_tables: torch.Tensor         # int32 [B, maxP]
     seq_lens: torch.Tensor             # int32 [B]
+    # varlen problems only: new tokens per sequence, and their row offsets
+    q_lens_host: np.ndarray | None = None      # int64 [B]
+    cu_seqlens: torch.Tensor | None = None     # int32 [B + 1]
 
     @property
     def B(self) -> int:
@@ -73,6 +78,8 @@ class Problem:
 
     @property
     def T(self) -> int:
+        if self.q_lens_host is not None:
+            return int(self.q_lens_host.sum())
         return self.B * self.q_len
 
     @property
@@ -95,12 +102,17 @@ def make_problem(name, Hq, Hkv, D, block_size, seq_lens, q_len, num_blocks,
 
     seq_lens counts the q_len new tokens; the new tokens of sequence b sit at
     positions seq_len - q_len .. seq_len - 1 and are given slots in the
-    sequence's own pages.  Physical blocks are a seeded random permutation of
-    [0, num_blocks); unused table entries are -1.
+    sequence's own pages.  q_len is one count for every sequence or (varlen)
+    one per sequence; varlen problems pack the new tokens back to back and
+    carry their row offsets (cu_seqlens).  Physical blocks are a seeded random
+    permutation of [0, num_blocks); unused table entries are -1.
     """
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int64)
     B = seq_lens.shape[0]
+    varlen = not np.isscalar(q_len)
+    q_lens = np.asarray(q_len, np.int64) if varlen else np.full(B, int(q_len), np.int64)
+    assert q_lens.shape == (B,) and np.all(q_lens >= 0) and np.all(q_lens <= seq_lens)
     pages = [_pages(n, block_size) for n in seq_lens]
     need = int(sum(pages))
     assert need <= num_blocks, (need, num_blocks)
@@ -113,18 +125,19 @@ def make_problem(name, Hq, Hkv, D, block_size, seq_lens, q_len, num_blocks,
         bt[b, :p] = ids[cur:cur + p]
         cur += p
     positions = np.concatenate(
-        [np.arange(n - q_len, n, dtype=np.int64) for n in seq_lens]
+        [np.arange(n - ql, n, dtype=np.int64) for n, ql in zip(seq_lens, q_lens)]
     ) if B else np.zeros(0, np.int64)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int64)
     slots = np.empty_like(positions)
     for b in range(B):
-        for t in range(q_len):
-            n = int(positions[b * q_len + t])
-            slots[b * q_len + t] = int(bt[b, n // block_size]) * block_size + n % block_size
+        for t in range(int(q_lens[b])):
+            n = int(positions[cu[b] + t])
+            slots[cu[b] + t] = int(bt[b, n // block_size]) * block_size + n % block_size
 
     dev = torch.device(device)
     g = torch.Generator(device=dev)
     g.manual_seed(int(seed))
-    T = B * q_len
+    T = int(cu[-1])
 
     def randn(*shape):
         return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
@@ -143,7 +156,8 @@ def make_problem(name, Hq, Hkv, D, block_size, seq_lens, q_len, num_blocks,
         k_cache[s:e] = torch.randn(e - s, block_size, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
         v_cache[s:e] = torch.randn(e - s, block_size, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
     return Problem(
-        name=name, Hq=Hq, Hkv=Hkv, D=D, block_size=block_size, q_len=q_len,
+        name=name, Hq=Hq, Hkv=Hkv, D=D, block_size=block_size,
+        q_len=int(q_lens.max()) if (varlen and B) else int(q_len) if not varlen else 0,
         seq_lens_host=seq_lens, block_tables_host=bt, num_blocks=num_blocks,
         theta=theta, eps=eps, q=q, k=k, v=v, gamma_q=gamma_q, gamma_k=gamma_k,
         positions=torch.from_numpy(positions).to(dev),
@@ -151,6 +165,8 @@ def make_problem(name, Hq, Hkv, D, block_size, seq_lens, q_len, num_blocks,
         k_cache=k_cache, v_cache=v_cache,
         block_tables=torch.from_numpy(bt).to(dev),
         seq_lens=torch.from_numpy(seq_lens.astype(np.int32)).to(dev),
+        q_lens_host=q_lens if varlen else None,
+        cu_seqlens=torch.from_numpy(cu.astype(np.int32)).to(dev) if varlen else None,
     )
 
 
@@ -213,3 +229,17 @@ def chunked_prefill(device="cpu", seed=BASE_SEED + 5, batch=8, chunk=512, lo=0, 
     nb = int(sum(_pages(n, block_size) for n in seq_lens)) + extra_blocks
     return make_problem(f"chunked_prefill_b{batch}_c{chunk}", Hq, Hkv, 128, block_size,
                         seq_lens, chunk, nb, seed, device)
+
+
+def varlen_prefill(device="cpu", seed=BASE_SEED + 6, batch=16, lo=128, hi=2048, prior_lo=0,
+                   prior_hi=0, Hq=16, Hkv=8, block_size=16):
+    """16q/8kv, D=128: `batch` prompts of U[lo, hi] new tokens each (varlen,
+    packed), after a prior context U[prior_lo, prior_hi] (0: fresh prompts);
+    cache = the pages needed, shuffled block ids."""
+    rng = np.random.default_rng(seed)
+    q_lens = rng.integers(lo, hi + 1, size=batch)
+    prior = rng.integers(prior_lo, prior_hi + 1, size=batch)
+    seq_lens = prior + q_lens
+    nb = max(1, int(sum(_pages(n, block_size) for n in seq_lens)))
+    return make_problem(f"varlen_prefill_b{batch}", Hq, Hkv, 128, block_size, seq_lens, q_lens,
+                        nb, seed, device)

@@ -195,3 +195,83 @@ def test_prefill_rejects_bad_arguments(lib):
         lib.paged_prefill(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
                           q_len=p.q_len, num_splits=3)       # no workspace
     assert e.value.status == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
+
+
+# ------------------------------------------------------------------ varlen
+
+def _varlen(lib, p, num_splits=1, hint=None, total_q=None):
+    total_q = p.T if total_q is None else total_q
+    out = torch.full((max(total_q, 1), p.Hq, p.D), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")[:total_q]
+    lse = torch.full((max(total_q, 1), p.Hq), float("nan"), device="cuda")[:total_q]
+    hint = p.max_seq_len if hint is None else hint
+    nbytes = lib.prefill_workspace_bytes(1, total_q, p.Hq, p.D, num_splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.paged_prefill_varlen(p.q, p.cu_seqlens, max(p.q_len, 1), p.k_cache, p.v_cache,
+                             p.block_tables, p.seq_lens, out, num_splits=num_splits,
+                             max_seq_len_hint=hint, lse_out=lse, workspace=ws,
+                             status_flags=flags)
+    torch.cuda.synchronize()
+    assert flags.item() == 0
+    return out, lse
+
+
+def _check_varlen(p, out, lse, what):
+    """Each sequence against the oracle run on that sequence alone."""
+    qb = bits(p.q)
+    cu = p.cu_seqlens.cpu().numpy()
+    for b in range(p.B):
+        ql = int(p.q_lens_host[b])
+        if ql == 0:
+            continue
+        kb, vb, table, lens = compact_cache(p, [b])
+        ref, ref_lse = oracle.paged_attention(qb[cu[b]:cu[b + 1]].reshape(1, ql, p.Hq, p.D), kb,
+                                              vb, table, lens, p.block_size, q_len=ql)
+        assert_attention_close(bits(out[cu[b]:cu[b + 1]]).reshape(1, ql, p.Hq, p.D), ref,
+                               lse[cu[b]:cu[b + 1]].cpu().numpy().reshape(1, ql, p.Hq), ref_lse,
+                               f"{what} seq {b} (q_len {ql}, keys {int(lens[0])})")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 4)])
+def test_varlen_prefill_matches_oracle(lib, Hq, Hkv):
+    # fresh prompts and later chunks mixed; lengths across row-tile edges
+    # (1, 64, 127/128/129 rows per kv head at group 2 and 8, 300, 700)
+    q_lens = [1, 64, 65, 128, 300, 7, 700, 33]
+    prior = [0, 0, 400, 0, 1000, 5, 0, 2500]
+    seq_lens = np.asarray(prior) + np.asarray(q_lens)
+    nb = int(sum(-(-int(n) // 16) for n in seq_lens))
+    p = workloads.make_problem("varlen", Hq, Hkv, 128, 16, seq_lens, q_lens, nb, 77, "cuda")
+    out, lse = _varlen(lib, p)
+    _check_varlen(p, out, lse, f"varlen Hq{Hq}/Hkv{Hkv}")
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_varlen_prefill_workload(lib, S):
+    p = workloads.varlen_prefill(device="cuda", batch=6, lo=100, hi=900, prior_hi=600)
+    out, lse = _varlen(lib, p, num_splits=S)
+    _check_varlen(p, out, lse, f"varlen workload S={S}")
+
+
+def test_varlen_equals_fixed_when_lengths_agree(lib):
+    # the same kernel arithmetic: varlen with equal lengths is bit-identical
+    # to the fixed-q_len entry point
+    p = _problem(16, 8, 150, 16, [0, 300, 77], seed=19)
+    p.q_lens_host = np.full(p.B, p.q_len, np.int64)
+    p.cu_seqlens = torch.arange(0, (p.B + 1) * p.q_len, p.q_len, dtype=torch.int32,
+                                device="cuda")
+    out_f, lse_f = _prefill(lib, p)
+    out_v, lse_v = _varlen(lib, p)
+    assert torch.equal(out_v, out_f.reshape(p.T, p.Hq, p.D))
+    assert torch.equal(lse_v, lse_f.reshape(p.T, p.Hq))
+
+
+def test_varlen_empty_sequences_and_short_grid(lib):
+    # zero-token sequences write nothing; max_q_len covers the longest
+    q_lens = [0, 5, 0, 260]
+    seq_lens = np.asarray([10, 5, 0, 300])
+    p = workloads.make_problem("varlen0", 16, 8, 128, 16, seq_lens, q_lens,
+                               int(sum(-(-int(n) // 16) for n in seq_lens)), 5, "cuda")
+    out, lse = _varlen(lib, p)
+    _check_varlen(p, out, lse, "varlen with empty sequences")
+    assert torch.isfinite(out.float()).all()
