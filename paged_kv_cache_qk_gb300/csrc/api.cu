@@ -8,6 +8,7 @@
 #include "pkvqk.h"
 #include "kernels.h"
 #include "prefill.h"
+#include "rope_math.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -15,6 +16,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -496,6 +498,10 @@ pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_strid
   a.eps = eps;
   for (int i = 0; i < 64; ++i)
     a.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
+  static float s_tab[pkvqk::kSinCosKnots][4];
+  static std::once_flag s_tab_once;
+  std::call_once(s_tab_once, [] { pkvqk::build_sincos_table(s_tab); });
+  std::memcpy(a.sincos_tab, s_tab, sizeof(s_tab));
   a.num_tokens = num_tokens;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = L.num_kv_heads;

@@ -22,6 +22,7 @@ struct NormRopeAppendArgs {
   const __nv_bfloat16* gamma_k;
   float eps;
   double inv_freq[64];             // theta^(-2i/D), i < D/2, computed on the host in float64
+  float sincos_tab[51][4];         // sin/cos(k/64) as float-float pairs (rope_math.cuh)
   int32_t num_tokens, num_q_heads, num_kv_heads;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;

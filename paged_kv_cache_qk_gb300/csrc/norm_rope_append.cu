@@ -9,19 +9,24 @@
 // one ulp of the correctly rounded exact value even where the rotation
 // cancels (y_i cos - y_{i+D/2} sin close to 0):
 //  * the token's 64 angles pos * inv_freq_i (inv_freq from the host, float64)
-//    are reduced by 2*pi in float64 and their sin/cos evaluated once per token
-//    to ~2e-14 (rope_math.cuh: Taylor series, float64 leading terms, float32
-//    tails), then kept in shared memory as float-float pairs (hi + lo);
+//    are formed and reduced by quarter turns in float64, and their sin/cos
+//    evaluated once per token in float-float arithmetic on the float32 pipe
+//    to ~2e-14 (rope_math.cuh: a 51-knot table and the addition theorems),
+//    one angle per lane of warps 0 and 1, then kept in shared memory as
+//    float-float pairs (hi + lo);
 //  * per element a = x * gamma is exact in fp32 (two 8-bit significands);
 //    the rotation a_i c - a_j s is formed with error-free products
 //    (p = a*c_hi, e = fma(a, c_hi, -p)) so cancellation loses nothing;
 //  * the RMS scale r = rsqrt(mean(x^2) + eps) multiplies the rotated value
 //    last (a common factor, it contributes only relative error).
-// Each head vector (D = 128 bf16 = 256 B) is handled by a half-warp (one
-// half-warp per vector, so all q/k/v loads of the token are issued before the
-// float64 angle work): lane l holds elements [8l, 8l+8) as one 16-byte load;
-// the sum of squares is a 4-step xor-shuffle reduction inside the half-warp,
-// and the rotate-half partner of lane l is lane l ^ 8.
+// Each head vector (D = 128 bf16 = 256 B) is handled by a half-warp: lane l
+// holds elements [8l, 8l+8) as one 16-byte load; the sum of squares is a
+// 4-step xor-shuffle reduction inside the half-warp, and the rotate-half
+// partner of lane l is lane l ^ 8.  A half-warp takes up to kHoist vectors of
+// its token, and issues all their loads before the angle work.  Few tokens
+// (decode): one half-warp per vector, the shortest path per token.  Many
+// tokens (prefill chunks): three or more warps per token and up to four
+// vectors per half-warp, so several tokens per SM overlap their latencies.
 #include "device_common.cuh"
 #include "kernels.h"
 #include "rope_math.cuh"
@@ -30,10 +35,9 @@ namespace pkvqk {
 
 namespace {
 
-constexpr int kMaxThreads = 1024;
-constexpr double kTwoPiHi = 6.283185307179586232;          // 2*pi rounded to double
-constexpr double kTwoPiLo = 2.4492935982947064e-16;          // 2*pi - kTwoPiHi
-constexpr double kInvTwoPi = 0.15915494309189535;
+constexpr int kMaxThreads = 512;
+constexpr int kHoist = 4;            // vectors per half-warp whose loads go first
+constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
 
 struct Loaded {
   uint4 x, g, v;
@@ -114,7 +118,7 @@ __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t
 }
 
 __global__ void __launch_bounds__(kMaxThreads)
-norm_rope_append_kernel(NormRopeAppendArgs a) {
+norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   __shared__ float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
   __shared__ float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
 
@@ -133,23 +137,22 @@ norm_rope_append_kernel(NormRopeAppendArgs a) {
   // every independent global load first
   const int64_t pos = a.positions[t];
   const int64_t slot = a.slot_mapping[t];
-  const Loaded first = load_vector(a, t, h0, l);
+  Loaded in[kHoist];
+#pragma unroll
+  for (int p = 0; p < kHoist; ++p) in[p] = load_vector(a, t, h0 + p * vec_per_pass, l);
 
-  // the token's 64 angles, 16 per warp on warps 0..3 (all four schedulers'
-  // float64 pipes): float64 sin/cos, kept as float-float pairs
-  if (warp < 4 && lane < 16) {
-    const int i = warp * 16 + lane;
-    const double ang = static_cast<double>(pos) * a.inv_freq[i];
-    const double turns = rint(ang * kInvTwoPi);
-    double red = fma(-turns, kTwoPiHi, ang);             // Cody-Waite: 2*pi = hi + lo
-    red = fma(-turns, kTwoPiLo, red);                     // |red| <= pi (+ rounding)
-    double sn, cs;
-    sincos_reduced(red, &sn, &cs);
-    const float ch = static_cast<float>(cs), sh = static_cast<float>(sn);
-    s_cos_hi[i] = ch;
-    s_cos_lo[i] = static_cast<float>(cs - static_cast<double>(ch));
-    s_sin_hi[i] = sh;
-    s_sin_lo[i] = static_cast<float>(sn - static_cast<double>(sh));
+  // the token's 64 angles, one per lane of warps 0 and 1 (every lane of a
+  // float64 instruction busy): float64 angle and quarter-turn reduction,
+  // float-float sin/cos
+  if (warp < 2) {
+    const int i = threadIdx.x;
+    FF x, sn, cs;
+    const int quadrant = reduce_angle(static_cast<double>(pos), a.inv_freq[i], &x);
+    sincos_ff(x, quadrant, a.sincos_tab, &sn, &cs);
+    s_cos_hi[i] = cs.hi;
+    s_cos_lo[i] = cs.lo;
+    s_sin_hi[i] = sn.hi;
+    s_sin_lo[i] = sn.lo;
   }
   const int64_t nslots = a.num_blocks * static_cast<int64_t>(a.block_size);
   if (threadIdx.x == 0 && slot >= nslots) report(a.status_flags, kFlagBadSlot);
@@ -159,11 +162,17 @@ norm_rope_append_kernel(NormRopeAppendArgs a) {
   const int64_t cache_row = blk * a.block_stride + off * a.slot_stride;
   __syncthreads();
 
-  finish_vector(a, t, h0, l, first, cache_row, write_cache, s_cos_hi, s_cos_lo, s_sin_hi,
-                s_sin_lo);
-  // more head vectors than half-warps (only when Hq + Hkv > 2 * warps)
+  // warp-uniform: both half-warps of a warp share `base`
   const int num_vec = a.num_q_heads + a.num_kv_heads;
-  for (int base = warp * 2 + vec_per_pass; base < num_vec; base += vec_per_pass) {
+#pragma unroll
+  for (int p = 0; p < kHoist; ++p) {
+    const int base = warp * 2 + p * vec_per_pass;
+    if (base < num_vec)
+      finish_vector(a, t, base + (lane >> 4), l, in[p], cache_row, write_cache, s_cos_hi,
+                    s_cos_lo, s_sin_hi, s_sin_lo);
+  }
+  // more head vectors than kHoist passes cover (Hq + Hkv > 2 * kHoist * warps)
+  for (int base = warp * 2 + kHoist * vec_per_pass; base < num_vec; base += vec_per_pass) {
     const int h = base + (lane >> 4);
     const Loaded in = load_vector(a, t, h, l);
     finish_vector(a, t, h, l, in, cache_row, write_cache, s_cos_hi, s_cos_lo, s_sin_hi,
@@ -175,10 +184,12 @@ norm_rope_append_kernel(NormRopeAppendArgs a) {
 
 cudaError_t launch_norm_rope_append(const NormRopeAppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
-  // one half-warp per head vector, at least 4 warps (the angle evaluation)
+  // few tokens: one half-warp per head vector; many: up to kHoist vectors per
+  // half-warp; at least 2 warps (one angle per lane of warps 0 and 1)
   const int num_vec = a.num_q_heads + a.num_kv_heads;
-  int warps = (num_vec + 1) / 2;
-  warps = warps < 4 ? 4 : (warps > kMaxThreads / 32 ? kMaxThreads / 32 : warps);
+  const int per_half_warp = a.num_tokens >= kManyTokens ? kHoist : 1;
+  int warps = (num_vec + 2 * per_half_warp - 1) / (2 * per_half_warp);
+  warps = warps < 2 ? 2 : (warps > kMaxThreads / 32 ? kMaxThreads / 32 : warps);
   return launch_pdl(norm_rope_append_kernel, dim3(a.num_tokens), dim3(warps * 32), 0, stream, a);
 }
 
