@@ -570,6 +570,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   __shared__ int issued;
   const int warp = threadIdx.x >> 5;
 
+  // launched as a programmatic dependent: q, the appended K/V, the tables and
+  // the lengths may come from the previous kernel in the stream
+  pdl_wait();
+  const Work w = decode_work(a);
+  // row tiles past this sequence's rows (varlen grids cover the longest
+  // sequence): nothing to compute or write; leave before any set-up
+  if (w.mt * 2 * kM >= w.rows) return;
+
   if (threadIdx.x == kProducerWarp * 32) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -591,10 +599,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
 
-  // launched as a programmatic dependent: q, the appended K/V, the tables and
-  // the lengths may come from the previous kernel in the stream
-  pdl_wait();
-  const Work w = decode_work(a);
   if (warp < 8) {
     // Q tiles: thread i loads row i % 128 of tile i / 128 (row = (token, q head
     // of the group)), two swizzled 64-dim halves
