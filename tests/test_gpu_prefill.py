@@ -275,3 +275,83 @@ def test_varlen_empty_sequences_and_short_grid(lib):
     out, lse = _varlen(lib, p)
     _check_varlen(p, out, lse, "varlen with empty sequences")
     assert torch.isfinite(out.float()).all()
+
+
+def _sampled_tokens(lib, p, out, lse, rng, per_seq=3):
+    """Sampled tokens of every sequence against the oracle's decode of that
+    token (query t of a q_len chunk sees the keys a single query at
+    seq_len - q_len + t + 1 sees)."""
+    qb = bits(p.q)
+    cu = (p.cu_seqlens.cpu().numpy() if p.cu_seqlens is not None
+          else np.arange(p.B + 1) * p.q_len)
+    q_lens = p.q_lens_host if p.q_lens_host is not None else np.full(p.B, p.q_len)
+    kb, vb, table, lens = compact_cache(p, list(range(p.B)))
+    for b in range(p.B):
+        ql = int(q_lens[b])
+        if ql == 0:
+            continue
+        for t in sorted(set([0, ql - 1] + list(rng.integers(0, ql, per_seq)))):
+            row = int(cu[b]) + t
+            ctx = int(lens[b]) - ql + t + 1
+            ref, ref_lse = oracle.paged_attention(qb[row:row + 1].reshape(1, 1, p.Hq, p.D), kb, vb,
+                                                  table[b:b + 1], np.array([ctx]), p.block_size)
+            assert_attention_close(bits(out[row:row + 1]).reshape(1, 1, p.Hq, p.D), ref,
+                                   lse[row:row + 1].cpu().numpy().reshape(1, 1, p.Hq), ref_lse,
+                                   f"b={b} t={t}")
+
+
+def test_prefill_4x2048_workload_sampled(lib):
+    """The 4 x 2048-token chunk workload in the benchmark's configuration."""
+    p = workloads.chunked_prefill(device="cuda", batch=4, chunk=2048, lo=0, hi=8192)
+    S = lib.choose_prefill_splits(p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
+    out, lse = _prefill(lib, p, num_splits=S)
+    _sampled_tokens(lib, p, out.reshape(p.T, p.Hq, p.D), lse.reshape(p.T, p.Hq),
+                    np.random.default_rng(45))
+
+
+def test_varlen_prefill_16_workload_sampled(lib):
+    """The varlen benchmark workload: 16 fresh prompts of U[128, 2048] tokens."""
+    p = workloads.varlen_prefill(device="cuda")
+    out, lse = _varlen(lib, p)
+    _sampled_tokens(lib, p, out, lse, np.random.default_rng(46), per_seq=2)
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_prefill_step_captures_and_replays(lib, S):
+    """Append + prefill record into a CUDA graph and replay bit-identically
+    (every call is host-decided and allocation-free)."""
+    p = workloads.chunked_prefill(device="cuda", batch=2, chunk=300, lo=100, hi=900)
+    nbytes = lib.prefill_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    q0, kc0, vc0 = p.q.clone(), p.k_cache.clone(), p.v_cache.clone()
+
+    def step(q, kc, vc, out, lse, stream):
+        lib.norm_rope_append(q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q, p.gamma_k,
+                             p.theta, p.eps, kc, vc, stream=stream)
+        lib.paged_prefill(q, kc, vc, p.block_tables, p.seq_lens, out, q_len=p.q_len,
+                          num_splits=S, max_seq_len_hint=p.max_seq_len, lse_out=lse,
+                          workspace=ws, stream=stream)
+
+    q_e, kc_e, vc_e = q0.clone(), kc0.clone(), vc0.clone()
+    out_e = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
+    lse_e = torch.empty(p.B, p.q_len, p.Hq, device="cuda")
+    step(q_e, kc_e, vc_e, out_e, lse_e, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    q_g, kc_g, vc_g = q0.clone(), kc0.clone(), vc0.clone()
+    out_g, lse_g = torch.zeros_like(out_e), torch.zeros_like(lse_e)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(q_g, kc_g, vc_g, out_g, lse_g, s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        q_g.copy_(q0)
+        kc_g.copy_(kc0)
+        vc_g.copy_(vc0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out_e) and torch.equal(lse_g, lse_e)
+        assert torch.equal(kc_g, kc_e) and torch.equal(q_g, q_e)
