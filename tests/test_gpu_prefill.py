@@ -355,3 +355,19 @@ def test_prefill_step_captures_and_replays(lib, S):
         torch.cuda.synchronize()
         assert torch.equal(out_g, out_e) and torch.equal(lse_g, lse_e)
         assert torch.equal(kc_g, kc_e) and torch.equal(q_g, q_e)
+
+
+def test_prefill_stacked_cache_and_strided_q(lib):
+    """K/V as strided views of one (num_blocks, 2, block_size, Hkv, D)
+    allocation, and q as the q part of a fused [tokens, Hq + 2 Hkv, D]
+    projection output: no copy of either is made."""
+    p = _problem(16, 8, 70, 16, [200, 0, 33], seed=61)
+    both = torch.stack([p.k_cache, p.v_cache], dim=1).contiguous()
+    qkv = torch.empty(p.T, p.Hq + 2 * p.Hkv, p.D, dtype=torch.bfloat16, device="cuda")
+    qkv[:, :p.Hq] = p.q
+    qkv[:, p.Hq:] = 7.0                           # k/v parts: must not be read as q
+    q_view = qkv[:, :p.Hq]
+    for S in (1, 2):
+        out, lse = _prefill(lib, p, num_splits=S, q=q_view, k_cache=both[:, 0],
+                            v_cache=both[:, 1])
+        _check_all(p, out, lse, f"stacked cache, strided q, S={S}")
