@@ -228,6 +228,24 @@ def run_cpu_baseline_child(seconds, max_seqs, ctx):
     return json.loads(r.stdout.decode().strip().splitlines()[-1])
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank values (every rank calls it; the result
+    is the same on all).  Single process: the values unchanged."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_rate(world, units_per_rank_step, ms_per_step):
+    """Whole-job rate of `world` replicas that each process
+    units_per_rank_step per step, timed by the slowest rank (units / s)."""
+    return world * units_per_rank_step / (ms_per_step * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -456,13 +474,10 @@ def main():
     clk = clocks.stop()
 
     ms = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
     bytes_step = decode_bytes + append_bytes
-    value = world * bytes_step / (ms * 1e-3) / 1e9
-    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+    value = aggregate_rate(world, bytes_step, ms) / 1e9
+    e2e_value = aggregate_rate(world, bytes_step, e2e_ms) / 1e9
 
     peak, peak_kind = load_peaks()
     rec = MEASURED_TRAFFIC.get(args.workload)
@@ -495,7 +510,7 @@ def main():
                   "L2 flushed (2x L2 write) before every step, excluded from timing",
             "parallelism": f"replicas x{world}",
         },
-        "seq_steps_per_s": round(world * p.B / (ms * 1e-3), 1),
+        "seq_steps_per_s": round(aggregate_rate(world, p.B, ms), 1),
         "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
@@ -523,15 +538,15 @@ def main():
         tpeak, tpeak_kind = load_peaks("bf16_tflops", 1900.0)
         tflops = flops / (dec_avg_ms * 1e-3) / 1e12
         line["metric"] = PREFILL_METRIC
-        line["value"] = round(world * flops / (ms * 1e-3) / 1e12, 2)
+        line["value"] = round(aggregate_rate(world, flops, ms) / 1e12, 2)
         line["unit"] = "TFLOP/s"
-        line["e2e"]["value"] = round(world * flops / (e2e_ms * 1e-3) / 1e12, 2)
+        line["e2e"]["value"] = round(aggregate_rate(world, flops, e2e_ms) / 1e12, 2)
         line["e2e"]["unit"] = "TFLOP/s"
         line["config"]["schedule"] = f"256-row CTA tiles (2 x 128, ping-pong) x split {S}"
         line["config"]["flops_per_step"] = flops
         line["config"]["kv_bytes_per_step"] = decode_bytes
         del line["pct_of_nominal_8tbs"]
-        line["tokens_per_s"] = round(world * p.T / (ms * 1e-3), 1)
+        line["tokens_per_s"] = round(aggregate_rate(world, p.T, ms), 1)
         line["roofline"] = {
             "kernel": "pkvqk_paged_prefill call: paged_prefill_kernel"
                       + (" + lse_combine_kernel" if S > 1 else ""),
