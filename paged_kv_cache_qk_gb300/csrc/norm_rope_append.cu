@@ -40,22 +40,20 @@ constexpr int kHoist = 4;            // vectors per half-warp whose loads go fir
 constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
 
 struct Loaded {
-  uint4 x, g, v;
+  uint4 x, v;
 };
 
-// Loads (x, gamma, and for k heads the v row) of head vector h of token t.
+// Loads x (and for k heads the v row) of head vector h of token t.
 __device__ __forceinline__ Loaded load_vector(const NormRopeAppendArgs& a, int t, int h, int l) {
   Loaded r;
-  r.x = r.g = r.v = make_uint4(0, 0, 0, 0);
+  r.x = r.v = make_uint4(0, 0, 0, 0);
   if (h < a.num_q_heads) {
     r.x = *reinterpret_cast<const uint4*>(a.q + t * a.q_stride_t +
                                           static_cast<int64_t>(h) * a.q_stride_h + l * 8);
-    r.g = __ldg(reinterpret_cast<const uint4*>(a.gamma_q + l * 8));
   } else if (h < a.num_q_heads + a.num_kv_heads) {
     const int hk = h - a.num_q_heads;
     r.x = __ldg(reinterpret_cast<const uint4*>(a.k + t * a.k_stride_t +
                                                static_cast<int64_t>(hk) * a.k_stride_h + l * 8));
-    r.g = __ldg(reinterpret_cast<const uint4*>(a.gamma_k + l * 8));
     r.v = __ldg(reinterpret_cast<const uint4*>(a.v + t * a.v_stride_t +
                                                static_cast<int64_t>(hk) * a.v_stride_h + l * 8));
   }
@@ -65,14 +63,15 @@ __device__ __forceinline__ Loaded load_vector(const NormRopeAppendArgs& a, int t
 // Norm + rotation + stores of one head vector; both half-warps of the warp
 // call it together (every shuffle is warp-wide).
 __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t, int h, int l,
-                                              const Loaded& in, int64_t cache_row,
+                                              const Loaded& in, const uint4& gq, const uint4& gk,
+                                              int64_t cache_row,
                                               bool write_cache, const float* s_cos_hi,
                                               const float* s_cos_lo, const float* s_sin_hi,
                                               const float* s_sin_lo) {
   const int num_vec = a.num_q_heads + a.num_kv_heads;
   float x[8], g[8];
   unpack8(in.x, x);
-  unpack8(in.g, g);
+  unpack8(h < a.num_q_heads ? gq : gk, g);
   // x*gamma is exact in fp32; x^2 is exact, the sum rounds
   float ss = 0.f, ag[8];
 #pragma unroll
@@ -140,6 +139,9 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   Loaded in[kHoist];
 #pragma unroll
   for (int p = 0; p < kHoist; ++p) in[p] = load_vector(a, t, h0 + p * vec_per_pass, l);
+  // the gains are the same for every token and head: one load per lane
+  const uint4 gq = __ldg(reinterpret_cast<const uint4*>(a.gamma_q + l * 8));
+  const uint4 gk = __ldg(reinterpret_cast<const uint4*>(a.gamma_k + l * 8));
 
   // the token's 64 angles, one per lane of warps 0 and 1 (every lane of a
   // float64 instruction busy): float64 angle and quarter-turn reduction,
@@ -168,14 +170,14 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   for (int p = 0; p < kHoist; ++p) {
     const int base = warp * 2 + p * vec_per_pass;
     if (base < num_vec)
-      finish_vector(a, t, base + (lane >> 4), l, in[p], cache_row, write_cache, s_cos_hi,
+      finish_vector(a, t, base + (lane >> 4), l, in[p], gq, gk, cache_row, write_cache, s_cos_hi,
                     s_cos_lo, s_sin_hi, s_sin_lo);
   }
   // more head vectors than kHoist passes cover (Hq + Hkv > 2 * kHoist * warps)
   for (int base = warp * 2 + kHoist * vec_per_pass; base < num_vec; base += vec_per_pass) {
     const int h = base + (lane >> 4);
     const Loaded in = load_vector(a, t, h, l);
-    finish_vector(a, t, h, l, in, cache_row, write_cache, s_cos_hi, s_cos_lo, s_sin_hi,
+    finish_vector(a, t, h, l, in, gq, gk, cache_row, write_cache, s_cos_hi, s_cos_lo, s_sin_hi,
                   s_sin_lo);
   }
 }
