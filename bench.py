@@ -254,43 +254,75 @@ def dist_env():
 
 
 def run_reference(args):
-    """Reference arm: the fp64 CPU oracle timed on the host cores."""
+    """Reference arm: the fp64 CPU oracle timed on the host cores.
+
+    Decode workloads: the oracle over one sequence of the workload's context
+    per step (GB/s).  Multi-query (prefill) workloads: the oracle over the
+    last tokens of one sequence's chunk, each with its whole causal context,
+    per step (TFLOP/s, the same algorithmic flop count as the GPU arm)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     name = args.workload
     builder, kw, desc = WORKLOADS[name]
-    ctx = kw.get("ctx", 8192)
-    # each step: the oracle over one sampled sequence of the workload's shape
     import numpy as np
     import torch
 
     import oracle
     from paged_kv_cache_qk_gb300 import workloads
 
-    seqs_per_step = 1
-    p = workloads.decode_uniform(seqs_per_step, ctx, device="cpu", seed=4242)
-    q = p.q.view(torch.int16).numpy().view(np.uint16).reshape(seqs_per_step, 1, p.Hq, p.D)
-    kb = p.k_cache.view(torch.int16).numpy().view(np.uint16)
-    vb = p.v_cache.view(torch.int16).numpy().view(np.uint16)
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    if name in PREFILL_WORKLOADS:
+        # one sequence of the workload, the last `tail` tokens of its chunk
+        p = getattr(workloads, builder)(device="cpu", **kw)
+        b = int(np.argmax(p.seq_lens_host))
+        q_lens = p.q_lens_host if p.q_lens_host is not None else np.full(p.B, p.q_len)
+        cu = np.concatenate([[0], np.cumsum(q_lens)])
+        tail = int(min(8, q_lens[b]))
+        L = int(p.seq_lens_host[b])
+        rows = u16(p.q)[cu[b] + q_lens[b] - tail: cu[b] + q_lens[b]].reshape(1, tail, p.Hq, p.D)
+        kb, vb = u16(p.k_cache), u16(p.v_cache)
+        table = p.block_tables_host[b:b + 1]
+        lens = np.array([L])
+
+        def once():
+            oracle.paged_attention(rows, kb, vb, table, lens, p.block_size, q_len=tail)
+        flops = 4 * p.D * p.Hq * sum(L - tail + t + 1 for t in range(tail))
+        sample = (f"sequence {b}: its last {tail} new tokens with {L - tail + 1}..{L} visible "
+                  f"keys each ({p.Hq}q/{p.Hkv}kv, D128) per step; numpy default threads")
+        metric, unit, scale = PREFILL_METRIC, "TFLOP/s", 1e12
+        work = flops
+    else:
+        ctx = kw.get("ctx", 8192)
+        seqs_per_step = 1
+        p = workloads.decode_uniform(seqs_per_step, ctx, device="cpu", seed=4242)
+        rows = u16(p.q).reshape(seqs_per_step, 1, p.Hq, p.D)
+        kb, vb = u16(p.k_cache), u16(p.v_cache)
+
+        def once():
+            oracle.paged_attention(rows, kb, vb, p.block_tables_host, p.seq_lens_host,
+                                   p.block_size)
+        sample = f"{seqs_per_step} sequence x ctx {ctx} (16q/8kv, D128) per step; numpy default threads"
+        metric, unit, scale = METRIC, "GB/s", 1e9
+        work = step_bytes(p)[0]
     for _ in range(args.warmup):
-        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
+        once()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
+        once()
     dt = (time.perf_counter() - t0) / max(1, args.steps)
-    nbytes = step_bytes(p)[0]
-    gbs = nbytes / dt / 1e9
+    rate = work / dt / scale
     line = {
-        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "impl": "reference", "metric": metric, "value": rate, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "sample": f"{seqs_per_step} sequence(s) x ctx {ctx} per step"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{seqs_per_step} sequence x ctx {ctx} (16q/8kv, D128) per step; "
-                                   "numpy default threads"},
-        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": desc, "sample": sample},
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
