@@ -159,8 +159,10 @@ PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
  *   [rows][num_splits][head_dim], then fp32 partial lse [rows][num_splits]
  *   (rows = (b*q_len + t)*Hq + h);
  * - num_splits == 0 (balanced): an upper bound for any kv-head count,
- *   ((SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded up, where
- *   SMs is the current device's multiprocessor count (internal layout).
+ *   (65536 + (SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded
+ *   up, where SMs is the current device's multiprocessor count: the 64 KiB
+ *   counter region (left as it is, so one workspace serves split and
+ *   balanced calls alike), then the partials (internal layout).
  */
 PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
                                     int32_t num_q_heads, int32_t head_dim,

@@ -156,14 +156,6 @@ int sm_count_current() {
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// Balanced schedule: fp32 partials [slot rows][128] + lse [slot rows], then
-// the int2 unit table [units].
-size_t balanced_bytes(int64_t slot_rows, int64_t units) {
-  const size_t raw = align16(static_cast<size_t>(slot_rows) * 129 * 4) +
-                     static_cast<size_t>(units) * 8;
-  return (raw + 255) & ~size_t(255);
-}
-
 // Split schedule: a fixed region of int32 arrival counters (one per unit,
 // never used for anything else, so calls of any shape can share one
 // workspace), then fp32 partials [rows][S][128] and partial lse [rows][S].
@@ -172,6 +164,16 @@ constexpr int64_t kMaxCounterUnits = kCounterBytes / 4;
 
 size_t partial_bytes(int64_t rows, int S) {
   const size_t raw = kCounterBytes + static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
+  return (raw + 255) & ~size_t(255);
+}
+
+// Balanced schedule: the counter region left untouched (so split and
+// balanced calls can share a workspace), then fp32 partials [slot rows][128]
+// and lse [slot rows] (slot = CTA + unit), then the int2 table [units] of the
+// first and last CTA of every unit.
+size_t balanced_bytes(int64_t slot_rows, int64_t units) {
+  const size_t raw = kCounterBytes + align16(static_cast<size_t>(slot_rows) * 129 * 4) +
+                     static_cast<size_t>(units) * 8;
   return (raw + 255) & ~size_t(255);
 }
 
@@ -288,10 +290,10 @@ pkvqk_status run_decode(const DecodeCall& c) {
   a.unit_info = nullptr;
   a.unit_counter = nullptr;
   if (S == 0) {
-    a.ws_o = static_cast<float*>(c.workspace);
+    char* base = static_cast<char*>(c.workspace) + kCounterBytes;
+    a.ws_o = reinterpret_cast<float*>(base);
     a.ws_lse = a.ws_o + slot_rows * 128;
-    a.unit_info = reinterpret_cast<int2*>(static_cast<char*>(c.workspace) +
-                                          align16(static_cast<size_t>(slot_rows) * 129 * 4));
+    a.unit_info = reinterpret_cast<int2*>(base + align16(static_cast<size_t>(slot_rows) * 129 * 4));
   } else if (need > 0) {
     a.unit_counter = static_cast<int32_t*>(c.workspace);
     a.ws_o = reinterpret_cast<float*>(static_cast<char*>(c.workspace) + kCounterBytes);

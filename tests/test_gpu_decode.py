@@ -304,3 +304,32 @@ def test_custom_scale(lib):
     out, lse, _ = _decode(lib, p, num_splits=0, scale=0.05)
     ref, ref_lse = oracle_attention(p, bits(p.q), scale=0.05)
     assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "scale 0.05")
+
+
+def test_workspace_shared_by_balanced_and_split_calls(lib):
+    """One workspace, zeroed once, across balanced and split calls of
+    different shapes: the split schedule's arrival counters sit in a fixed
+    region at the workspace start that balanced calls leave alone, and they
+    are back at zero after every split call (balanced partials once started
+    at offset 0, on top of those counters)."""
+    probs = [workloads.decode_uniform(8, 2048, device="cuda"),
+             workloads.make_problem("bal-mixed", 32, 4, 128, 16, [3000, 17, 900, 4100, 1], 1,
+                                    600, 818, "cuda"),
+             workloads.verify_causal(device="cuda", batch=6)]
+    nbytes = max(lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+                 for p in probs for S in (0, 3))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    # balanced calls of every shape, then again interleaved with split calls
+    # (both schedules keep their counters in the same region)
+    calls = [(p, 0) for p in probs] + [(p, S) for p in probs for S in (3, 0)]
+    for i, (p, S) in enumerate(calls):
+        out = torch.full((p.B, p.q_len, p.Hq, p.D), float("nan"), dtype=torch.bfloat16,
+                         device="cuda")
+        lse = torch.full((p.B, p.q_len, p.Hq), float("nan"), device="cuda")
+        lib.paged_decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                         q_len=p.q_len, num_splits=S, max_seq_len_hint=p.max_seq_len,
+                         lse_out=lse, workspace=ws)
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle_attention(p, bits(p.q))
+        assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse,
+                               f"workspace reuse call {i} ({p.name}, S={S})")
