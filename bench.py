@@ -420,8 +420,8 @@ def main():
 
     if prefill:   # append, prefill (+ lse combine when split)
         launches_per_step = 2 + (1 if S > 1 else 0)
-    else:         # append, decode (+ balanced combine)
-        launches_per_step = 2 + (1 if S == 0 else 0)
+    else:         # append, decode (+ the combine of the split or balanced partials)
+        launches_per_step = 2 + (1 if S != 1 else 0)
 
     for _ in range(args.warmup):
         step()
@@ -549,8 +549,8 @@ def main():
         "gpu_launches": K * launches_per_step,
         "roofline": {
             "kernel": "pkvqk_paged_decode call: paged_decode_kernel"
-                      + (" + balanced combine kernel" if S == 0 else
-                         " (split partials merged in-kernel)" if S > 1 else ""),
+                      + (" + balanced_combine_kernel" if S == 0 else
+                         " + lse_combine_kernel" if S > 1 else ""),
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": peak,

@@ -153,16 +153,14 @@ PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
 /*
  * Workspace bytes pkvqk_paged_decode needs on the current device:
  * - num_splits == 1: 0;
- * - num_splits >= 2: 65536 + batch*q_len*Hq*num_splits*(head_dim + 1)*4,
- *   rounded up to 256.  Layout: a 64 KiB region of int32 per-(sequence,
- *   kv-head group) arrival counters, then fp32 partial outputs
- *   [rows][num_splits][head_dim], then fp32 partial lse [rows][num_splits]
- *   (rows = (b*q_len + t)*Hq + h);
+ * - num_splits >= 2: batch*q_len*Hq*num_splits*(head_dim + 1)*4, rounded up
+ *   to 256.  Layout: fp32 partial outputs [rows][num_splits][head_dim], then
+ *   fp32 partial lse [rows][num_splits] (rows = (b*q_len + t)*Hq + h);
  * - num_splits == 0 (balanced): an upper bound for any kv-head count,
- *   (65536 + (SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded
- *   up, where SMs is the current device's multiprocessor count: the 64 KiB
- *   counter region (left as it is, so one workspace serves split and
- *   balanced calls alike), then the partials (internal layout).
+ *   ((SMs + batch)*q_len*Hq*(head_dim + 1)*4 + batch*Hq*8) rounded up, where
+ *   SMs is the current device's multiprocessor count (internal layout).
+ * Nothing in the workspace needs to start at zero, and calls of any shape and
+ * schedule may share one (in stream order).
  */
 PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
                                     int32_t num_q_heads, int32_t head_dim,
@@ -185,9 +183,9 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   block_size) / num_splits) pages, split j < S-1 of a sequence covers pages
  *   [j*C, (j+1)*C) and split S-1 covers [(S-1)*C, end), so every key is
  *   covered whatever the hint.  Each split keeps an online softmax; for
- *   num_splits > 1 the partials go to the workspace and the CTA that
- *   finishes a sequence's last split merges them by log-sum-exp inside the
- *   same kernel (it counts arrivals; no CTA waits for another).
+ *   num_splits > 1 the partials go to the workspace and a log-sum-exp
+ *   combine kernel that this call launches (as a programmatic dependent, so
+ *   its launch overlaps the decode kernel's tail) merges them.
  *   pkvqk_choose_num_splits gives a host-side choice.
  * - num_splits == 0 (balanced): one CTA per SM; the pages of all (sequence,
  *   kv-head group) pairs are laid end to end and every CTA takes an equal
@@ -204,11 +202,7 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   out           device bf16 [batch, q_len, Hq, head_dim], contiguous
  *   lse_out       device fp32 [batch, q_len, Hq] or NULL
  *   workspace     device, >= pkvqk_decode_workspace_bytes(batch, q_len, Hq,
- *                 head_dim, num_splits) on the current device (NULL if 0);
- *                 zero-filled before its first use (e.g. cudaMemsetAsync);
- *                 every call leaves it reusable without clearing (its
- *                 counters return to zero), unless a call reports
- *                 PKVQK_FLAG_WAIT_TIMEOUT
+ *                 head_dim, num_splits) on the current device (NULL if 0)
  * Supported: head_dim 128, Hq % Hkv == 0, q_len*Hq/Hkv <= 16.
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode(

@@ -156,23 +156,17 @@ int sm_count_current() {
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// Split schedule: a fixed region of int32 arrival counters (one per unit,
-// never used for anything else, so calls of any shape can share one
-// workspace), then fp32 partials [rows][S][128] and partial lse [rows][S].
-constexpr size_t kCounterBytes = 64 << 10;
-constexpr int64_t kMaxCounterUnits = kCounterBytes / 4;
-
+// Split schedule: fp32 partials [rows][S][128], then partial lse [rows][S].
 size_t partial_bytes(int64_t rows, int S) {
-  const size_t raw = kCounterBytes + static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
+  const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
   return (raw + 255) & ~size_t(255);
 }
 
-// Balanced schedule: the counter region left untouched (so split and
-// balanced calls can share a workspace), then fp32 partials [slot rows][128]
-// and lse [slot rows] (slot = CTA + unit), then the int2 table [units] of the
-// first and last CTA of every unit.
+// Balanced schedule: fp32 partials [slot rows][128] and lse [slot rows]
+// (slot = CTA + unit), then the int2 table [units] of the first and last CTA
+// of every unit.
 size_t balanced_bytes(int64_t slot_rows, int64_t units) {
-  const size_t raw = kCounterBytes + align16(static_cast<size_t>(slot_rows) * 129 * 4) +
+  const size_t raw = align16(static_cast<size_t>(slot_rows) * 129 * 4) +
                      static_cast<size_t>(units) * 8;
   return (raw + 255) & ~size_t(255);
 }
@@ -288,20 +282,15 @@ pkvqk_status run_decode(const DecodeCall& c) {
   a.ws_o = nullptr;
   a.ws_lse = nullptr;
   a.unit_info = nullptr;
-  a.unit_counter = nullptr;
   if (S == 0) {
-    char* base = static_cast<char*>(c.workspace) + kCounterBytes;
+    char* base = static_cast<char*>(c.workspace);
     a.ws_o = reinterpret_cast<float*>(base);
     a.ws_lse = a.ws_o + slot_rows * 128;
     a.unit_info = reinterpret_cast<int2*>(base + align16(static_cast<size_t>(slot_rows) * 129 * 4));
   } else if (need > 0) {
-    a.unit_counter = static_cast<int32_t*>(c.workspace);
-    a.ws_o = reinterpret_cast<float*>(static_cast<char*>(c.workspace) + kCounterBytes);
+    a.ws_o = static_cast<float*>(c.workspace);
     a.ws_lse = a.ws_o + nrows * S * 128;
   }
-  // merge in the decode kernel unless the caller wants the partials, or the
-  // units outnumber the counter region (then a separate combine kernel runs)
-  a.fuse_combine = (S > 1 && !c.partials_only && units <= kMaxCounterUnits) ? 1 : 0;
   a.status_flags = c.status_flags;
 
   cudaError_t e = pkvqk::launch_paged_decode(plan, kmap, vmap, a, grid_ctas, c.stream);
@@ -309,7 +298,7 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (S == 0) {
     e = pkvqk::launch_balanced_combine(a, plan.heads_per_cta, c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
-  } else if (S > 1 && !c.partials_only && !a.fuse_combine) {
+  } else if (S > 1 && !c.partials_only) {
     e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
                                   c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");

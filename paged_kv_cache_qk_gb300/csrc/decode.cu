@@ -762,42 +762,6 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
 
 // --------------------------------------------------- in-kernel LSE combine
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-// Split schedule: the CTA that finishes last among the num_splits CTAs of a
-// (sequence, head group) unit merges the unit's partials into the output and
-// resets the unit's counter (the next call finds it at zero again).  Called
-// by the consumer warps once their partials are written; no CTA waits for
-// another.
-template <int HPC>
-__device__ void merge_if_last(const DecodeArgs& a, int* last_cta) {
-  const int nthreads = HPC * 32;
-  __threadfence();                                  // this thread's partial stores
-  consumer_sync(nthreads);
-  const int b = blockIdx.z, hg = blockIdx.y;
-  const int u = hg * a.batch + b;
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(&a.unit_counter[u], 1);
-    *last_cta = (old == a.num_splits - 1);
-  }
-  consumer_sync(nthreads);
-  if (!*last_cta) return;
-  __threadfence();                                  // see the other CTAs' partials
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = a.num_splits;
-  for (int r = warp; r < a.rows_per_unit; r += HPC) {
-    // unit row r = (t * HPC + hh) * group + gi
-    const int gi = r % a.group, th = r / a.group, hh = th % HPC, t = th / HPC;
-    const int h = (hg * HPC + hh) * a.group + gi;
-    const long long row = (static_cast<long long>(b) * a.q_len + t) * a.num_q_heads + h;
-    combine_row<true>(a.ws_o, a.ws_lse, row * S, 1, S, a.out + row * kHeadDim,
-                      a.lse_out != nullptr ? a.lse_out + row : nullptr, lane);
-  }
-  if (threadIdx.x == 0) a.unit_counter[u] = 0;
-}
-
 // ------------------------------------------------------------------ kernel
 
 template <int HPC, int TK, int BUDGET, int R, bool TC>
@@ -814,7 +778,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   __shared__ int issued;
   __shared__ Plan plan;
   __shared__ long long wsum[32];
-  __shared__ int last_cta;
   uint8_t* stages = align1024(smem_raw);
 
   const int warp = threadIdx.x >> 5;
@@ -847,7 +810,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       consume_simt<HPC, TK, BUDGET, STAGES, R>(a, &plan, stages, full, empty, &abort_flag);
     }
   }
-  if (a.fuse_combine && warp < kProducer) merge_if_last<HPC>(a, &last_cta);
   __syncthreads();
   if (abort_flag && threadIdx.x == kProducer * 32) drain<STAGES>(full, issued);
 }

@@ -53,8 +53,6 @@ struct DecodeArgs {
   float* ws_o;                   // partial outputs (split / balanced schedules)
   float* ws_lse;                 // partial lse
   int2* unit_info;               // balanced: first and last CTA of every (seq, group) unit
-  int32_t* unit_counter;         // split, merged in-kernel: arrivals per (seq, group) unit
-  int32_t fuse_combine;          // split schedule: the last CTA of a unit merges its partials
   int32_t* status_flags;
 };
 

@@ -118,8 +118,8 @@ def test_workspace_bytes_formula(lib):
     assert lib.decode_workspace_bytes(4, 1, 16, 128, 1) == 0
     assert lib.decode_workspace_bytes(4, 1, 16, 128, 0) > 0       # balanced schedule bound
     for B, T, Hq, S in [(4, 1, 16, 4), (64, 1, 16, 19), (32, 5, 16, 8), (1, 1, 8, 2)]:
-        # 64 KiB of counters, then partials [rows][S][128] + lse [rows][S]
-        raw = 65536 + B * T * Hq * S * 129 * 4
+        # partials [rows][S][128] + lse [rows][S]
+        raw = B * T * Hq * S * 129 * 4
         assert lib.decode_workspace_bytes(B, T, Hq, 128, S) == (raw + 255) // 256 * 256
     assert lib.decode_workspace_bytes(4, 1, 16, 64, 4) == 0
 
