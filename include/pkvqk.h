@@ -142,8 +142,11 @@ PKVQK_API pkvqk_status pkvqk_norm_rope_append(
  * read): batch, kv heads, rows per kv head (q_len * Hq/Hkv), the longest
  * sequence, the total key count and the SM count (0 = query the current
  * device).  Returns 0 (the balanced schedule: chosen for large batches of
- * mixed lengths) or a split count in [1, 256].  Source: the "decode routing
- * hint (host side, zero device sync)" of InfiniLM PR #585, Summary item 3.
+ * mixed lengths) or a split count in [1, 256]; above 16 rows per kv head
+ * (run on the tensor-core kernel, see pkvqk_paged_decode) it returns
+ * pkvqk_choose_prefill_splits(batch, num_kv_heads, rows_per_kv_head, 1, ...).
+ * Source: the "decode routing hint (host side, zero device sync)" of
+ * InfiniLM PR #585, Summary item 3.
  */
 PKVQK_API int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads,
                                 int32_t rows_per_kv_head, int32_t max_seq_len,
@@ -203,7 +206,12 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   lse_out       device fp32 [batch, q_len, Hq] or NULL
  *   workspace     device, >= pkvqk_decode_workspace_bytes(batch, q_len, Hq,
  *                 head_dim, num_splits) on the current device (NULL if 0)
- * Supported: head_dim 128, Hq % Hkv == 0, q_len*Hq/Hkv <= 16.
+ * Supported: head_dim 128, Hq % Hkv == 0, q_len <= 16.  Up to 16 rows per
+ * kv head (q_len*Hq/Hkv) run on the decode kernel; more (e.g. q_len 5 at
+ * 8 q heads per kv head) run on the tensor-core multi-query kernel of
+ * pkvqk_paged_prefill with the same split boundaries and partial layout,
+ * and num_splits == 0 there becomes a split count whose partials fit the
+ * balanced workspace bound.
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,

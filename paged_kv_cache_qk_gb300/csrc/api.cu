@@ -191,6 +191,8 @@ struct DecodeCall {
   bool partials_only;
 };
 
+pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64_t total_q);
+
 pkvqk_status run_decode(const DecodeCall& c) {
   PKVQK_TRY(check_layout(c.layout));
   const pkvqk_cache_layout& L = *c.layout;
@@ -201,8 +203,6 @@ pkvqk_status run_decode(const DecodeCall& c) {
                 c.num_q_heads, L.num_kv_heads);
   const int group = c.num_q_heads / L.num_kv_heads;
   const int rows = c.q_len * group;
-  if (rows > 16)
-    return fail(PKVQK_ERR_UNSUPPORTED, "q_len * group = %d rows per kv head (max 16)", rows);
   if (c.max_blocks_per_seq < 1) return fail(PKVQK_ERR_INVALID_ARG, "max_blocks_per_seq < 1");
   if (c.max_seq_len_hint < 0) return fail(PKVQK_ERR_INVALID_ARG, "max_seq_len_hint < 0");
   if (c.num_splits < 0 || c.num_splits > 256)
@@ -212,6 +212,23 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (c.q_stride_t % 8 || c.q_stride_h % 8 || c.q_stride_h < 1 || c.q_stride_t < 0)
     return fail(PKVQK_ERR_INVALID_ARG, "q strides must be multiples of 8 elements");
   if (!std::isfinite(c.scale)) return fail(PKVQK_ERR_INVALID_ARG, "scale is not finite");
+  if (rows > 16) {
+    // More query rows per kv head than the decode kernel's register tiles
+    // hold: the tensor-core multi-query kernel computes the same rows, with
+    // the same split boundaries and partial layout.  The balanced schedule
+    // has no counterpart there; it becomes a split count whose partials fit
+    // the balanced workspace bound ((SMs + batch) x q_len x Hq rows).
+    DecodeCall p = c;
+    if (p.num_splits == 0) {
+      const int64_t cap = static_cast<int64_t>(c.max_blocks_per_seq) * L.block_size;
+      const int hint = c.max_seq_len_hint > 0
+                           ? c.max_seq_len_hint
+                           : static_cast<int>(std::min<int64_t>(cap, INT32_MAX));
+      const int S = pkvqk_choose_prefill_splits(c.batch, L.num_kv_heads, c.q_len, group, hint, 0);
+      p.num_splits = std::max(1, std::min(S, 1 + sm_count_current() / std::max(1, c.batch)));
+    }
+    return run_prefill(p, nullptr, static_cast<int64_t>(c.batch) * c.q_len);
+  }
 
   const int64_t cap_tokens = static_cast<int64_t>(c.max_blocks_per_seq) * L.block_size;
   const int hint = c.max_seq_len_hint > 0
@@ -364,10 +381,12 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
   PKVQK_TRY(check_device_ptr(c.block_tables, "block_tables"));
   PKVQK_TRY(check_device_ptr(c.seq_lens, "seq_lens"));
   if (cu_seqlens_q != nullptr) PKVQK_TRY(check_device_ptr(cu_seqlens_q, "cu_seqlens_q"));
-  PKVQK_TRY(check_device_ptr(c.out, "out"));
-  if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
-  if (!aligned16(c.q) || !aligned16(c.out))
-    return fail(PKVQK_ERR_INVALID_ARG, "q/out not 16-byte aligned");
+  if (!c.partials_only) {
+    PKVQK_TRY(check_device_ptr(c.out, "out"));
+    if (c.lse_out != nullptr) PKVQK_TRY(check_device_ptr(c.lse_out, "lse_out"));
+    if (!aligned16(c.out)) return fail(PKVQK_ERR_INVALID_ARG, "out not 16-byte aligned");
+  }
+  if (!aligned16(c.q)) return fail(PKVQK_ERR_INVALID_ARG, "q not 16-byte aligned");
   if (!aligned16(c.k_cache) || !aligned16(c.v_cache))
     return fail(PKVQK_ERR_INVALID_ARG, "cache base not 16-byte aligned");
   if (need > 0) {
@@ -414,7 +433,7 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
 
   cudaError_t e = pkvqk::launch_paged_prefill(kmap, vmap, a, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
-  if (S > 1) {
+  if (S > 1 && !c.partials_only) {
     e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,
                                   c.stream);
     if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
@@ -514,6 +533,11 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
                                 int32_t sm_count) {
   if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0 || block_size <= 0) return 1;
   if (sm_count <= 0) sm_count = sm_count_current();
+  // pkvqk_paged_decode runs more than 16 rows per kv head on the tensor-core
+  // multi-query kernel: its own choice (rows = q_len * group with group 1)
+  if (rows_per_kv_head > 16)
+    return pkvqk_choose_prefill_splits(batch, num_kv_heads, rows_per_kv_head, 1, max_seq_len,
+                                       sm_count);
   const pkvqk::DecodePlan plan = pkvqk::plan_decode(num_kv_heads, rows_per_kv_head);
   const int64_t groups = num_kv_heads / plan.heads_per_cta;
   const int64_t p_max = (max_seq_len + block_size - 1) / block_size;

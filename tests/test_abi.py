@@ -68,7 +68,13 @@ def test_decode_validation_errors(lib):
     assert _decode(lib, lay, q_len=0) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, q_len=17) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, Hq=12) == lib.PKVQK_ERR_INVALID_ARG            # 12 % 8 != 0
-    assert _decode(lib, lay, Hq=64, q_len=3) == lib.PKVQK_ERR_UNSUPPORTED   # 24 rows per kv head
+    # 24 rows per kv head take the tensor-core route, which checks its own
+    # workspace need (rows x splits x 129 x 4 bytes) before any pointer
+    assert _decode(lib, lay, Hq=64, q_len=3, S=4, ws=100) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
+    # the balanced schedule there becomes a split count (> 1 for 32 CTAs
+    # over 8192 keys), whose partials need a workspace too
+    assert _decode(lib, lay, Hq=64, q_len=3, S=0, ws=100, hint=8192,
+                   maxp=512) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
     assert _decode(lib, lay, S=257) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, S=-1) == lib.PKVQK_ERR_INVALID_ARG
     assert _decode(lib, lay, S=0, ws=100) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
@@ -139,3 +145,14 @@ def test_split_heuristic_is_host_only_and_bounded(lib):
     assert lib.choose_num_splits(32, 8, 10, 8197, 172000, 16, 152) == 0
     # small mixed batch: still a split count
     assert lib.choose_num_splits(4, 8, 2, 256, 600, 16, 152) >= 1
+
+
+def test_split_heuristic_above_16_rows_is_the_tensor_core_choice(lib):
+    # above 16 rows per kv head pkvqk_paged_decode runs the multi-query
+    # tensor-core kernel, so the chooser gives that kernel's split count
+    # (never the balanced schedule, which that kernel does not have)
+    for B, hkv, rows, L in [(4, 8, 40, 8192), (1, 8, 24, 512), (64, 8, 40, 16384),
+                            (32, 4, 128, 8197)]:
+        S = lib.choose_num_splits(B, hkv, rows, L, B * L // 2, 16, 152)
+        assert S == lib.choose_prefill_splits(B, hkv, rows, 1, L, 152)
+        assert S >= 1

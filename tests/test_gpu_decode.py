@@ -142,6 +142,43 @@ def test_multi_query_small_all_rows(lib, q_len, Hq, Hkv):
         _check(p, out, lse, what=f"q_len={q_len} Hq={Hq} Hkv={Hkv} S={S}")
 
 
+@pytest.mark.parametrize("q_len,Hq,Hkv", [(5, 64, 8), (3, 48, 8), (16, 32, 8), (9, 16, 8)])
+def test_multi_query_beyond_16_rows_all_rows(lib, q_len, Hq, Hkv):
+    # more than 16 rows per kv head (18 .. 128): the call runs on the
+    # tensor-core multi-query kernel; every schedule argument stays valid
+    lens = [q_len, q_len + 1, 16 + q_len, 300, 37, 129 + q_len]
+    p = workloads.make_problem("mq16", Hq, Hkv, 128, 16, lens, q_len, 40, 930 + q_len, "cuda")
+    rows = q_len * Hq // Hkv
+    assert rows > 16
+    for S in (0, 1, 3, -1):
+        out, lse, S_used = _decode(lib, p, num_splits=S)
+        assert S_used >= 1 or S == 0
+        _check(p, out, lse, what=f"q_len={q_len} Hq={Hq} Hkv={Hkv} S={S_used}")
+
+
+def test_partials_beyond_16_rows_equal_decode(lib):
+    # the tensor-core route writes the decode kernel's partial layout, so
+    # partials + pkvqk_lse_combine reproduce the merged call bit for bit
+    q_len, Hq, Hkv, S = 5, 64, 8, 3
+    p = workloads.make_problem("mq16p", Hq, Hkv, 128, 16, [5, 300, 77, 1000], q_len, 100, 941,
+                               "cuda")
+    out, lse, _ = _decode(lib, p, num_splits=S)
+    nbytes = lib.decode_workspace_bytes(p.B, q_len, p.Hq, p.D, S)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    lib.paged_decode_partials(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, ws,
+                              q_len=q_len, num_splits=S, max_seq_len_hint=p.max_seq_len)
+    rows = p.B * q_len * p.Hq
+    ws_f = ws.view(torch.float32)
+    ws_o = ws_f[: rows * S * 128]
+    ws_lse = ws_f[rows * S * 128: rows * S * 129]
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    lib.lse_combine(ws_o, ws_lse, rows, S, out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    _check(p, out2, lse2, what="partials + combine, 40 rows per kv head")
+
+
 def test_edge_lengths_and_empty_sequence(lib):
     # seq_len 0 -> zeros and -inf; lengths at tile / page boundaries
     lens = [0, 1, 15, 16, 17, 31, 32, 33, 255, 256]
