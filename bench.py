@@ -51,6 +51,8 @@ WORKLOADS = {
 }
 WORKLOADS["decode_gqa8_64x4096"] = ("make_problem_uniform_gqa8", {},
                                     "GQA-8 decode 32q/4kv D128 bs16, batch 64 x ctx 4096 (uniform)")
+WORKLOADS["decode_gqa4_32x8192"] = ("make_problem_uniform_gqa4", {},
+                                    "Qwen3-8B decode 32q/8kv D128 bs16, batch 32 x ctx 8192 (uniform)")
 # the tensor-core multi-query kernel (pkvqk_paged_prefill): chunked prefill,
 # and the verify shape through the same kernel
 PREFILL_WORKLOADS = {
@@ -370,6 +372,10 @@ def main():
         import numpy as _np
         p = workloads.make_problem("gqa8_uniform", 32, 4, 128, 16, _np.full(64, 4096), 1,
                                    64 * 256, workloads.BASE_SEED + 3, device=dev)
+    elif builder == "make_problem_uniform_gqa4":
+        import numpy as _np
+        p = workloads.make_problem("gqa4_uniform", 32, 8, 128, 16, _np.full(32, 8192), 1,
+                                   32 * 512, workloads.BASE_SEED + 7, device=dev)
     else:
         p = getattr(workloads, builder)(device=dev, **kw)
     decode_bytes, append_bytes = step_bytes(p)

@@ -546,13 +546,18 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
   // fastest with ~0.84 x (resident CTA slots) CTAs in flight -- enough to
   // saturate HBM, one wave so no straggler wave -- and with the longest
   // sequence cut finely enough that its chunk is no larger than the average
-  // CTA's share; chunks under 128 keys cost more in start-up than they gain.
+  // CTA's share; chunks under 128 keys cost more in start-up than they gain,
+  // except on short contexts (<= 2048 keys), where 64-key chunks spread the
+  // few CTAs' work wider (1 x 512: 17.1 -> 15.0 us, 1 x 2048: 19.1 -> 17.1).
   const double target = 0.84 * sm_count * plan.ctas_per_sm;
   const int64_t s_fill = static_cast<int64_t>(target / static_cast<double>(groups * batch) + 0.5);
-  const int64_t s_bal =
-      static_cast<int64_t>(std::ceil(static_cast<double>(p_max) * target / static_cast<double>(tp)));
+  // (a CTA covers one head group: tp * groups pages of work in all)
+  const int64_t s_bal = static_cast<int64_t>(
+      std::ceil(static_cast<double>(p_max) * target / (static_cast<double>(tp) * groups)));
   int64_t S = std::max<int64_t>(1, std::max(s_fill, s_bal));
-  const int64_t s_min_chunk = std::max<int64_t>(1, (p_max * block_size + 127) / 128);
+  const int64_t min_chunk = p_max * block_size <= 2048 ? 64 : 128;
+  const int64_t s_min_chunk =
+      std::max<int64_t>(1, (p_max * block_size + min_chunk - 1) / min_chunk);
   S = std::min<int64_t>(S, std::min<int64_t>(s_min_chunk, std::min<int64_t>(p_max, 256)));
   // drop splits that the longest sequence leaves empty
   const int64_t chunk = (p_max + S - 1) / S;

@@ -26,13 +26,18 @@
 // full/empty mbarriers; the ring runs on across segments.  Warps 0..HPC-1
 // consume, one per kv head, every q row that reads their kv head
 // (rows = q_len * group):
-//   * rows <= 4 ("simt"): 8 lanes per key, 4 keys per warp instruction; each
-//     lane holds 16 of the 128 dims, the q.k dot is a 3-step xor-shuffle
-//     reduction; every 8-lane key group keeps its own online softmax and the
-//     four groups are merged by shuffles at the end of a segment.
-//   * rows 5..16 ("tc"): the 16 padded rows x 16 keys score tile and the
-//     16 rows x 128 dims output tile are mma.sync m16n8k16 bf16 contractions
-//     fed by ldmatrix from the swizzled stages (conflict-free).
+//   * rows <= 2 ("simt", GQA-2 and multi-head decode): 8 lanes per key, 4
+//     keys per warp instruction; each lane holds 16 of the 128 dims, the q.k
+//     dot is a 3-step xor-shuffle reduction; every 8-lane key group keeps
+//     its own online softmax and the four groups are merged by shuffles at
+//     the end of a segment.
+//   * rows 3..16 ("tc", GQA-4 and GQA-8 decode, verify): the 16 padded rows
+//     x 16 keys score tile and the 16 rows x 128 dims output tile are
+//     mma.sync m16n8k16 bf16 contractions fed by ldmatrix from the swizzled
+//     stages (conflict-free).  From 3 rows on the per-row dot products make
+//     the CUDA-core form issue-bound below the HBM rate (measured on GB300,
+//     32 x 8192 at 4 rows: 255 us with one warp per kv head, 225 us with
+//     two; mma tiles 166 us, the HBM bound).
 // Every wait on an mbarrier is bounded; on a timeout the CTA reports
 // PKVQK_FLAG_WAIT_TIMEOUT, drains its own copies in flight and exits.
 #include "combine_row.cuh"
@@ -760,7 +765,40 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
   }
 }
 
-// --------------------------------------------------- in-kernel LSE combine
+// Before the dependency wait the previous kernel (the append) is still
+// running and HBM is mostly idle: start this CTA's first ring of K/V tiles
+// (split schedule), or the line(s) of sequence lengths the plan reads
+// (balanced schedule), towards L2.  A prefetch binds no value -- the loads
+// after the wait read L2, which the previous kernel's writes update -- so a
+// block table or length that the previous kernel rewrites costs only a wasted
+// prefetch.  The two values read here go through L2 only (ld.global.cg), so
+// no L1 copy of them outlives the wait.
+template <int HPC, int TK, int NT>
+__device__ void prefetch_before_wait(const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                     const DecodeArgs& a) {
+  const int lane = threadIdx.x & 31;
+  if (a.num_splits == 0) {
+    for (int i = lane * 32; i < a.batch; i += 32 * 32) prefetch_l2(a.seq_lens + i);
+    return;
+  }
+  if (lane >= NT) return;
+  const int b = blockIdx.z, hg = blockIdx.y, j = blockIdx.x;
+  const long long cap = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+  long long L = __ldcg(a.seq_lens + b);
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const long long chunk = static_cast<long long>(a.chunk_pages) * a.block_size;
+  const long long k0 = static_cast<long long>(j) * chunk;
+  const long long k1 = (j == a.num_splits - 1) ? L : min(L, k0 + chunk);
+  const long long key = k0 + static_cast<long long>(lane) * TK;
+  if (key >= k1) return;
+  const long long page = key / a.block_size;
+  const int blk = __ldcg(a.block_tables + static_cast<long long>(b) * a.max_blocks_per_seq + page);
+  if (blk < 0 || blk >= a.num_blocks) return;
+  const int slot = static_cast<int>(key - page * a.block_size);
+  tma_prefetch_5d(kmap, 0, slot, 0, hg * HPC, blk);
+  tma_prefetch_5d(vmap, 0, slot, 0, hg * HPC, blk);
+}
+
 
 // ------------------------------------------------------------------ kernel
 
@@ -784,12 +822,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], HPC);
+      mbar_init(&empty[s], Geo::kConsumers);
     }
     abort_flag = 0;
     issued = 0;
     fence_barrier_init();
   }
+  if (warp == kProducer) prefetch_before_wait<HPC, TK, STAGES>(&kmap, &vmap, a);
   __syncthreads();
   // launched as a programmatic dependent: everything below may read what the
   // previous kernel in the stream wrote (q, appended K/V, tables, lengths)
@@ -861,8 +900,6 @@ cudaError_t launch_hpc(const DecodePlan& p, const CUtensorMap& kmap, const CUten
   switch (p.rows) {
     case 1: return launch_one<HPC, TK, B, 1, false>(kmap, vmap, a, grid_ctas, stream);
     case 2: return launch_one<HPC, TK, B, 2, false>(kmap, vmap, a, grid_ctas, stream);
-    case 3: return launch_one<HPC, TK, B, 3, false>(kmap, vmap, a, grid_ctas, stream);
-    case 4: return launch_one<HPC, TK, B, 4, false>(kmap, vmap, a, grid_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -888,7 +925,7 @@ DecodePlan plan_decode(int num_kv_heads, int rows) {
   int hpc = 8;
   while (hpc > 1 && (num_kv_heads % hpc) != 0) hpc >>= 1;
   p.heads_per_cta = hpc;
-  p.tensor_core = rows > 4;
+  p.tensor_core = rows > 2;
   p.rows = rows;
   switch (hpc) {
     case 8: fill_plan<8>(p); break;

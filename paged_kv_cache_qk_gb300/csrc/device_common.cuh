@@ -116,6 +116,23 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Prefetch of one 5-D box of a tensor map into L2 (nothing lands in shared
+// memory, nothing is counted on a barrier; boxes outside the tensor fetch
+// nothing).
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
+// Prefetch of the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-
 // swizzled sub-tile whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {

@@ -59,7 +59,7 @@ struct DecodeArgs {
 // Kernel family chosen by the host for a decode call.
 struct DecodePlan {
   int heads_per_cta;   // kv heads handled by one CTA (divides num_kv_heads)
-  bool tensor_core;    // mma tiles (rows per kv head > 4) vs CUDA-core dots
+  bool tensor_core;    // mma tiles (rows per kv head > 2) vs CUDA-core dots
   int rows;            // q_len * group
   int tile_keys;       // keys per TMA tile (8 or 16)
   int ctas_per_sm;     // resident CTAs per SM the shared-memory ring allows

@@ -11,9 +11,9 @@
 //  * the token's 64 angles pos * inv_freq_i (inv_freq from the host, float64)
 //    are formed and reduced by quarter turns in float64, and their sin/cos
 //    evaluated once per token in float-float arithmetic on the float32 pipe
-//    to ~2e-14 (rope_math.cuh: a 51-knot table and the addition theorems),
-//    one angle per lane of warps 0 and 1, then kept in shared memory as
-//    float-float pairs (hi + lo);
+//    to ~2e-14 (rope_math.cuh: a 51-knot table, copied to shared memory
+//    first, and the addition theorems), one angle per lane of warps 0 and 1,
+//    then kept in shared memory as float-float pairs (hi + lo);
 //  * per element a = x * gamma is exact in fp32 (two 8-bit significands);
 //    the rotation a_i c - a_j s is formed with error-free products
 //    (p = a*c_hi, e = fma(a, c_hi, -p)) so cancellation loses nothing;
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kMaxThreads)
 norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   __shared__ float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
   __shared__ float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
+  __shared__ float s_tab[kSinCosKnots][4];
 
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5;
@@ -142,6 +143,13 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   // the gains are the same for every token and head: one load per lane
   const uint4 gq = __ldg(reinterpret_cast<const uint4*>(a.gamma_q + l * 8));
   const uint4 gk = __ldg(reinterpret_cast<const uint4*>(a.gamma_k + l * 8));
+  // the sin/cos knots to shared memory while those loads are in flight: the
+  // lookups below take a different knot in every lane, and indexing the
+  // parameter copy that way costs one constant-cache access per distinct
+  // address (cold misses included) on the angle's critical path
+  for (int e = threadIdx.x; e < kSinCosKnots * 4; e += blockDim.x)
+    (&s_tab[0][0])[e] = (&a.sincos_tab[0][0])[e];
+  __syncthreads();
 
   // the token's 64 angles, one per lane of warps 0 and 1 (every lane of a
   // float64 instruction busy): float64 angle and quarter-turn reduction,
@@ -150,7 +158,7 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
     const int i = threadIdx.x;
     FF x, sn, cs;
     const int quadrant = reduce_angle(static_cast<double>(pos), a.inv_freq[i], &x);
-    sincos_ff(x, quadrant, a.sincos_tab, &sn, &cs);
+    sincos_ff(x, quadrant, s_tab, &sn, &cs);
     s_cos_hi[i] = cs.hi;
     s_cos_lo[i] = cs.lo;
     s_sin_hi[i] = sn.hi;

@@ -132,9 +132,11 @@ def test_verify_causal_sampled(lib):
         _check(p, out, lse, seqs=[0, 9, 31], what=f"verify S={S_used}")
 
 
-@pytest.mark.parametrize("q_len,Hq,Hkv", [(5, 16, 8), (2, 16, 8), (3, 8, 8), (4, 32, 8), (2, 32, 4)])
+@pytest.mark.parametrize("q_len,Hq,Hkv", [(5, 16, 8), (2, 16, 8), (3, 8, 8), (4, 32, 8), (2, 32, 4),
+                                           (1, 8, 8), (1, 24, 8)])
 def test_multi_query_small_all_rows(lib, q_len, Hq, Hkv):
-    # rows per kv head = q_len * group covers both kernel families (<=4 and 5..16)
+    # rows per kv head = q_len * group covers both kernel families (1..2:
+    # CUDA cores; 3..16: mma tiles), including one row (MHA) and 3 rows
     lens = [q_len, q_len + 1, 16 + q_len, 100, 37]
     p = workloads.make_problem("mq", Hq, Hkv, 128, 16, lens, q_len, 40, 906 + q_len, "cuda")
     for S in (0, 1, 2):
