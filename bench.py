@@ -86,7 +86,7 @@ for _b in (1, 8, 32, 64):
 # kernel sources it was taken with: when the sources hash differently, the
 # bench reports traffic as null.
 MEASURED_TRAFFIC = {
-    "decode_64x8192": {"src": "e883b5d0d6682187", "bytes": 2149602944, "num_splits": 2},
+    "decode_64x8192": {"src": "c1195e589950f770", "bytes": 2149463936, "num_splits": 2},
 }
 
 

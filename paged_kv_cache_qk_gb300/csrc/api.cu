@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -49,6 +50,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // device-resident arguments are checked before use).
 pkvqk_status check_device_ptr(const void* p, const char* name) {
   if (p == nullptr) return fail(PKVQK_ERR_INVALID_ARG, "%s is NULL", name);
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) cur = -1;
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, p);
   if (e != cudaSuccess) {
@@ -58,10 +61,9 @@ pkvqk_status check_device_ptr(const void* p, const char* name) {
   }
   if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
     return fail(PKVQK_ERR_POINTER_RESIDENCY, "%s is not device memory", name);
-  int dev = -1;
-  if (cudaGetDevice(&dev) == cudaSuccess && attr.type == cudaMemoryTypeDevice && attr.device != dev)
+  if (cur >= 0 && attr.type == cudaMemoryTypeDevice && attr.device != cur)
     return fail(PKVQK_ERR_POINTER_RESIDENCY, "%s lives on device %d, current device is %d", name,
-                attr.device, dev);
+                attr.device, cur);
   return PKVQK_OK;
 }
 
@@ -143,14 +145,17 @@ pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_ca
 // ---------------------------------------------------------------- SM count
 
 int sm_count_current() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64] = {};      // 0 = not queried yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     n = 148;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -858,8 +858,8 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
                        int grid_ctas, cudaStream_t stream) {
   using Geo = Geometry<HPC, TK, BUDGET>;
   auto kern = paged_decode_kernel<HPC, TK, BUDGET, R, TC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Geo::kSmemBytes);
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(kern, Geo::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid = a.num_splits == 0 ? dim3(grid_ctas, 1, 1)
                                       : dim3(a.num_splits, a.num_kv_heads / HPC, a.batch);

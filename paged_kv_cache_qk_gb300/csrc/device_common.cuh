@@ -4,6 +4,8 @@
 // unpacking and the tile geometry of the paged K/V stage buffers.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -16,6 +18,22 @@ namespace pkvqk {
 // Launch with programmatic stream serialization: the kernel may begin while
 // the previous kernel in the stream finishes; it calls pdl_wait() before
 // touching anything that kernel may have written.
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current
+// device once: `done` (one per kernel instance) keeps a bit per device (the
+// attribute belongs to the device's context; setting it twice is harmless,
+// so racing threads need no lock).
+template <typename K>
+inline cudaError_t set_smem_limit_once(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args&&... args) {

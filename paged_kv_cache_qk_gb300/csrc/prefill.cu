@@ -652,8 +652,8 @@ int prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillArgs& a, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(paged_prefill_kernel, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const long long gx = static_cast<long long>(a.m_tiles) * a.num_kv_heads * a.num_splits;
   return launch_pdl(paged_prefill_kernel, dim3(static_cast<unsigned>(gx), a.batch),

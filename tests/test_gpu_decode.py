@@ -368,3 +368,25 @@ def test_workspace_shared_by_balanced_and_split_calls(lib):
         ref, ref_lse = oracle_attention(p, bits(p.q))
         assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse,
                                f"workspace reuse call {i} ({p.name}, S={S})")
+
+
+def test_host_pointer_rejected_after_device_calls(lib):
+    """The residency check (pageable host memory where device memory is
+    expected) fires on every call, also right after successful device calls,
+    and a rejected call launches nothing."""
+    p = workloads.decode_tiny(device="cuda")
+    out, lse, _ = _decode(lib, p, num_splits=1)
+    _check(p, out, lse, what="before the host-pointer call")
+    for host_arg in ("q", "seq_lens"):
+        kw = {"q": p.q, "seq_lens": p.seq_lens}
+        kw[host_arg] = kw[host_arg].cpu()
+        out2 = torch.full_like(out, float("nan"))
+        with pytest.raises(lib.PkvqkError) as ei:
+            lib.paged_decode(kw["q"], p.k_cache, p.v_cache, p.block_tables, kw["seq_lens"], out2,
+                             q_len=p.q_len, num_splits=1, max_seq_len_hint=p.max_seq_len)
+        assert ei.value.status == lib.PKVQK_ERR_POINTER_RESIDENCY
+        torch.cuda.synchronize()
+        assert torch.isnan(out2.float()).all()
+    # the same device pointers still pass afterwards
+    out3, lse3, _ = _decode(lib, p, num_splits=1)
+    assert torch.equal(out3, out)
