@@ -8,7 +8,15 @@ is above 1, the LSE combine (pkvqk_lse_combine) — all through the C ABI.
 
 Default workload: Qwen3-0.6B decode, 16 q / 8 kv heads, head_dim 128, bf16,
 block_size 16, batch 64 x context 8192, shuffled block ids (2.15 GB of K/V
-per step, larger than L2, so no flush is needed between steps).
+per step, larger than L2, so no flush is needed between steps).  Workloads
+under 4x L2 start every step from a cold, clean L2: 2x L2 written, then 2x L2
+read (the written lines go back to HBM before the step, not inside it).
+
+Timing: pass 1 times K steps issued back to back with no event between the
+calls of a step (the `value`); pass 2 times the same K steps with events
+around each call (the per-call durations of `roofline`); the `e2e` pass adds
+every step's host-to-device input copy and device-to-host output copy,
+pipelined on their own streams.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle as reference arm
@@ -86,7 +94,7 @@ for _b in (1, 8, 32, 64):
 # kernel sources it was taken with: when the sources hash differently, the
 # bench reports traffic as null.
 MEASURED_TRAFFIC = {
-    "decode_64x8192": {"src": "c1195e589950f770", "bytes": 2149463936, "num_splits": 2},
+    "decode_64x8192": {"src": "c083c8138855a550", "bytes": 2149280512, "num_splits": 2},
 }
 
 
@@ -398,18 +406,27 @@ def main():
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     big_inputs = decode_bytes > 4 * l2_bytes
     flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+    flush_clean = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8,
+                                                      device=dev)
 
-    def decode_call(qq, bt, sl, cu=None):
+    def cold_l2():
+        # write 2x L2 (evicts every input line), then read another 2x L2 so
+        # the written lines go back to HBM here and not inside the next step
+        flush.zero_()
+        flush_clean.max()
+
+    def decode_call(qq, bt, sl, cu=None, o=None):
+        o = out if o is None else o
         if varlen:
             lib.paged_prefill_varlen(qq, p.cu_seqlens if cu is None else cu, p.q_len,
-                                     p.k_cache, p.v_cache, bt, sl, out, num_splits=S,
+                                     p.k_cache, p.v_cache, bt, sl, o, num_splits=S,
                                      max_seq_len_hint=p.max_seq_len, workspace=ws, stream=stream)
         elif prefill:
-            lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len,
+            lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
                               num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
                               stream=stream)
         else:
-            lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, out, q_len=p.q_len,
+            lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
                              num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
                              stream=stream)
 
@@ -429,19 +446,22 @@ def main():
     else:         # append, decode (+ the combine of the split or balanced partials)
         launches_per_step = 2 + (1 if S != 1 else 0)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-
+    # the clock sampler starts (and settles) before the warm-up, so that the
+    # warm-up, not an idle pause, is what directly precedes the timed steps
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")
                           if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
                           else f"/tmp/pkvqk_bench_clocks_r{rank}.csv")
     time.sleep(0.3)
 
-    K = args.steps
+    for _ in range(args.warmup):
+        if not big_inputs:
+            cold_l2()
+        step()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    K = args.steps
     # Pass 1, the step value: K steps as a caller issues them, with no event
     # between the calls of a step (an event recorded between two kernels ends
     # the programmatic-dependent overlap of the second one's launch and
@@ -459,7 +479,7 @@ def main():
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(K)]
         for i in range(K):
-            flush.zero_()
+            cold_l2()
             step_ev[i][0].record(stream)
             step()
             step_ev[i][1].record(stream)
@@ -472,7 +492,7 @@ def main():
     evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     for i in range(K):
         if not big_inputs:
-            flush.zero_()
+            cold_l2()
         step(evs[i])
     torch.cuda.synchronize()
     append_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -502,23 +522,52 @@ def main():
     d2h = host_out.numel() * host_out.element_size()
     K_e2e = max(3, min(K, 500))
 
-    def e2e_step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        lib.norm_rope_append(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["positions"],
-                             dev_in["slot_mapping"], p.gamma_q, p.gamma_k, p.theta, p.eps,
-                             p.k_cache, p.v_cache, stream=stream)
-        decode_call(dev_in["q"], dev_in["block_tables"], dev_in["seq_lens"],
-                    dev_in.get("cu_seqlens"))
-        host_out.copy_(out, non_blocking=True)
+    # Pipelined as a serving loop runs it: step i's inputs go up on an upload
+    # stream and its output comes back on a readback stream while the compute
+    # stream works on the neighbouring steps; two input and two output buffers
+    # alternate, and events order every reuse.  Each step still moves its own
+    # inputs and output inside the timed region.
+    dev_bufs = [dev_buf, torch.empty_like(dev_buf)]
+    dev_ins = [dev_in, {n: dev_bufs[1][o:o + nb].view(dt).view(shp)
+                        for n, (o, nb, dt, shp) in fields.items()}]
+    outs = [out, torch.empty_like(out)]
+    host_outs = [host_out, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    read_back = [torch.cuda.Event() for _ in range(2)]
+    for ev in computed + read_back:
+        ev.record(stream)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_step(i):
+        k = i & 1
+        with torch.cuda.stream(up):
+            up.wait_event(computed[k])           # step i - 2 is done reading buffer k
+            dev_bufs[k].copy_(host_buf, non_blocking=True)
+            uploaded[k].record(up)
+        stream.wait_event(uploaded[k])
+        stream.wait_event(read_back[k])          # step i - 2's output has left outs[k]
+        d = dev_ins[k]
+        lib.norm_rope_append(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"],
+                             p.gamma_q, p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache,
+                             stream=stream)
+        decode_call(d["q"], d["block_tables"], d["seq_lens"], d.get("cu_seqlens"), outs[k])
+        computed[k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[k])
+            host_outs[k].copy_(outs[k], non_blocking=True)
+            read_back[k].record(down)
+
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K_e2e):
-        e2e_step()
+    for i in range(K_e2e):
+        e2e_step(i)
+    for ev in read_back:
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K_e2e
@@ -558,13 +607,15 @@ def main():
             "schedule": "balanced (one CTA per SM)" if S == 0 else f"split x{S}",
             "l2": ("inputs larger than L2: %.2f GB of K/V per step vs %d MB L2" %
                    (decode_bytes / 1e9, l2_bytes >> 20)) if big_inputs else
-                  "L2 flushed (2x L2 write) before every step, excluded from timing",
+                  "L2 flushed before every step (2x L2 written, then 2x L2 read so the "
+                  "written lines are back in HBM before the step), excluded from timing",
             "parallelism": f"replicas x{world}",
         },
         "seq_steps_per_s": round(aggregate_rate(world, p.B, ms), 1),
         "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                "copies": "pipelined: upload and readback streams, double-buffered"},
         "gpu_launches": K * launches_per_step,
         "roofline": {
             "kernel": "pkvqk_paged_decode call: paged_decode_kernel"

@@ -30,7 +30,7 @@ lse_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
-  combine_row<false>(ws_o, ws_lse, row * S, 1, S, out + row * kHeadDim,
+  combine_row(ws_o, ws_lse, row * S, 1, S, out + row * kHeadDim,
               lse_out != nullptr ? lse_out + row : nullptr, lane);
 }
 
@@ -55,7 +55,7 @@ balanced_combine_kernel(const DecodeArgs a, int hpc) {
   if (info.x == info.y) return;                 // written whole by one CTA
   const long long srow = (t * hpc + hh) * a.group + gi;
   const long long base = (static_cast<long long>(info.x) + u) * a.rows_per_unit + srow;
-  combine_row<false>(a.ws_o, a.ws_lse, base, a.rows_per_unit, info.y - info.x + 1,
+  combine_row(a.ws_o, a.ws_lse, base, a.rows_per_unit, info.y - info.x + 1,
               a.out + row * kHeadDim, a.lse_out != nullptr ? a.lse_out + row : nullptr, lane);
 }
 

@@ -1,5 +1,5 @@
 // Log-sum-exp merge of split-KV partials for one output row (one warp),
-// shared by the combine kernels and by the decode kernel's in-kernel merge.
+// shared by the split and the balanced combine kernels.
 //
 // Operation: InfiniLM PR #585 "perf: Qwen3 offline inference — hybrid
 // attention backend, ...", section "概述 / Summary", item 1 ("splitkv"): the
@@ -17,16 +17,14 @@ namespace pkvqk {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Merge of n partial rows at ws index base + j * stride (j < n) into one
-// bf16 output row (+ lse); one warp.
-template <bool kFresh>
+// bf16 output row (+ lse); one warp.  The partials come from the previous
+// kernel in the stream, so the read-only path may cache them.
 __device__ __forceinline__ void combine_row(const float* __restrict__ ws_o,
                                             const float* __restrict__ ws_lse, long long base,
                                             long long stride, int n, __nv_bfloat16* out_row,
                                             float* lse_dst, int lane) {
-  // kFresh: the partials were written by other CTAs of the running kernel,
-  // so they are read through L2 (ld.global.cg), never the read-only path
-  auto ld_part = [](const float* ptr) { return kFresh ? __ldcg(ptr) : __ldg(ptr); };
-  auto ld_part4 = [](const float4* ptr) { return kFresh ? __ldcg(ptr) : __ldg(ptr); };
+  auto ld_part = [](const float* ptr) { return __ldg(ptr); };
+  auto ld_part4 = [](const float4* ptr) { return __ldg(ptr); };
   // pass 1: the row's max lse (lane j holds split j, j + 32, ...)
   float M = -INFINITY;
   for (int j = lane; j < n; j += 32) M = fmaxf(M, ld_part(ws_lse + base + j * stride));

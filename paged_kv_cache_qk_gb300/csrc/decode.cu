@@ -52,24 +52,6 @@ namespace {
 
 constexpr float kLn2 = 0.693147180559945309f;
 
-// Tile / ring choices per kv-head group size (measured on GB300; see the
-// notes in Config below).
-#ifndef PKVQK_HPC8_SIMT_TK
-#define PKVQK_HPC8_SIMT_TK 16
-#endif
-#ifndef PKVQK_HPC8_SIMT_BUDGET
-#define PKVQK_HPC8_SIMT_BUDGET 192
-#endif
-#ifndef PKVQK_HPC8_TC_BUDGET
-#define PKVQK_HPC8_TC_BUDGET 192
-#endif
-#ifndef PKVQK_HPC4_BUDGET
-#define PKVQK_HPC4_BUDGET 192
-#endif
-#ifndef PKVQK_TC_ILP
-#define PKVQK_TC_ILP 0
-#endif
-
 // HPC kv heads per CTA, TK keys per tile (one TMA box covers TK consecutive
 // slots of a page), stage ring of at most BUDGET_KB kilobytes.
 template <int HPC, int TK, int BUDGET_KB>
@@ -83,7 +65,6 @@ struct Geometry {
   static constexpr int kConsumers = HPC;
   static constexpr int kThreads = (kConsumers + 1) * 32;
 };
-
 
 constexpr int kDestFinal = 0;   // bf16 output + lse
 constexpr int kDestSplit = 1;   // partial at [row][split] (split schedule)
@@ -650,30 +631,16 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
       const uint32_t vt = kt + HPC * kHeadTileBytes;
       const int key0 = seg.k0 + i * TK;
 
-      // S (16 rows x 16 keys) = Q K^T; even and odd k-steps accumulate
-      // separately (two chains of 4 instead of one of 8)
+      // S (16 rows x 16 keys) = Q K^T over 8 k-steps of 16 dims
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int key = ((mat >> 1) << 3) + mrow;
         const int ch = 2 * kk + (mat & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kt + (ch >> 3) * kHalfTileBytes + swz128(key, ch & 7), b0, b1, b2, b3);
-        if (PKVQK_TC_ILP && (kk & 1)) {
-          mma_bf16(sd[0], qa[kk], b0, b1);
-          mma_bf16(sd[1], qa[kk], b2, b3);
-        } else {
-          mma_bf16(sc[0], qa[kk], b0, b1);
-          mma_bf16(sc[1], qa[kk], b2, b3);
-        }
-      }
-      if (PKVQK_TC_ILP) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sc[0][e] += sd[0][e];
-          sc[1][e] += sd[1][e];
-        }
+        mma_bf16(sc[0], qa[kk], b0, b1);
+        mma_bf16(sc[1], qa[kk], b2, b3);
       }
 
 #pragma unroll
@@ -732,7 +699,6 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-
 
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
     lA += __shfl_xor_sync(0xffffffffu, lA, 2);
@@ -798,7 +764,6 @@ __device__ void prefetch_before_wait(const CUtensorMap* kmap, const CUtensorMap*
   tma_prefetch_5d(kmap, 0, slot, 0, hg * HPC, blk);
   tma_prefetch_5d(vmap, 0, slot, 0, hg * HPC, blk);
 }
-
 
 // ------------------------------------------------------------------ kernel
 
@@ -871,13 +836,13 @@ template <int HPC>
 struct Config;
 template <>
 struct Config<8> {
-  static constexpr int kSimtTK = PKVQK_HPC8_SIMT_TK, kSimtBudget = PKVQK_HPC8_SIMT_BUDGET;
-  static constexpr int kTcBudget = PKVQK_HPC8_TC_BUDGET;
+  static constexpr int kSimtTK = 16, kSimtBudget = 192;
+  static constexpr int kTcBudget = 192;
 };
 template <>
 struct Config<4> {
-  static constexpr int kSimtTK = 16, kSimtBudget = PKVQK_HPC4_BUDGET;
-  static constexpr int kTcBudget = PKVQK_HPC4_BUDGET;
+  static constexpr int kSimtTK = 16, kSimtBudget = 192;
+  static constexpr int kTcBudget = 192;
 };
 template <>
 struct Config<2> {
