@@ -128,6 +128,13 @@ def test_workspace_bytes_formula(lib):
         raw = B * T * Hq * S * 129 * 4
         assert lib.decode_workspace_bytes(B, T, Hq, 128, S) == (raw + 255) // 256 * 256
     assert lib.decode_workspace_bytes(4, 1, 16, 64, 4) == 0
+    # balanced bound: ((SMs + batch) q_len Hq (D + 1) 4 + batch Hq 8), the first
+    # part 16-byte aligned, rounded up to 256; without a GPU the library assumes
+    # 148 SMs
+    for B, T, Hq in [(4, 1, 16), (64, 1, 32), (32, 5, 16), (1, 1, 8)]:
+        doc = (148 + B) * T * Hq * 129 * 4 + B * Hq * 8
+        got = lib.decode_workspace_bytes(B, T, Hq, 128, 0)
+        assert doc <= got <= doc + 16 + 255 and got % 256 == 0
 
 
 def test_split_heuristic_is_host_only_and_bounded(lib):

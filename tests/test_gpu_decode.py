@@ -390,3 +390,32 @@ def test_host_pointer_rejected_after_device_calls(lib):
     # the same device pointers still pass afterwards
     out3, lse3, _ = _decode(lib, p, num_splits=1)
     assert torch.equal(out3, out)
+
+
+def test_balanced_schedule_any_workspace_contents(lib):
+    """Whatever the workspace holds before a balanced-schedule call (all
+    ones, random bytes, a previous call's partials and unit table), the
+    result is the same and matches the oracle."""
+    lens = list(np.random.default_rng(951).integers(1, 3000, size=24))
+    p = workloads.make_problem("bal_ws", 32, 4, 128, 16, lens, 1, 24 * 190, 951, "cuda")
+    nbytes = lib.decode_workspace_bytes(p.B, 1, p.Hq, p.D, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ref, ref_lse = oracle_attention(p, bits(p.q))
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    fills = ["ones", "random", "reuse", "reuse"]
+    prev = None
+    for fill in fills:
+        if fill == "ones":
+            ws.fill_(0xFF)
+        elif fill == "random":
+            ws.copy_(torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda",
+                                   generator=gen))
+        out = torch.full((p.B, 1, p.Hq, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((p.B, 1, p.Hq), float("nan"), device="cuda")
+        lib.paged_decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out,
+                         num_splits=0, max_seq_len_hint=p.max_seq_len, lse_out=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, f"balanced ws {fill}")
+        if prev is not None:
+            assert torch.equal(out, prev)        # the page partition fixes every bit
+        prev = out
