@@ -90,13 +90,37 @@ def test_decode_uniform_small_points_all_rows(lib, batch, ctx):
 
 
 def test_decode_uniform_64x8192_sampled(lib):
-    """The benchmark workload (64 x 8192, heuristic split count), 6 sampled
-    sequences compared in full."""
+    """The benchmark workload (64 x 8192) on the balanced schedule, 6 sampled
+    sequences compared in full (the split schedule the benchmark times is
+    covered by the sweep test below)."""
     p = workloads.decode_uniform(64, 8192, device="cuda")
     out, lse, S = _decode(lib, p, num_splits=0)
     seqs = sorted(np.random.default_rng(5).choice(64, 6, replace=False).tolist())
     _check(p, out, lse, seqs=seqs, what=f"64x8192 S={S}")
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("batch,ctx", [(b, c) for b in (1, 8, 32, 64) for c in (512, 2048, 8192)])
+def test_decode_sweep_point_in_bench_configuration(lib, batch, ctx):
+    """Every point of the batch x context sweep in the launch configuration
+    the benchmark times (the split heuristic's count): the first, the last
+    and one seeded sequence compared in full."""
+    p = workloads.decode_uniform(batch, ctx, device="cuda")
+    out, lse, S = _decode(lib, p, num_splits=-1)
+    pick = int(np.random.default_rng(batch * 131 + ctx).integers(batch))
+    seqs = sorted({0, batch - 1, pick})
+    _check(p, out, lse, seqs=seqs, what=f"{batch}x{ctx} S={S}")
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,B,ctx,seed", [
+    ("gqa8_uniform", 32, 4, 64, 4096, 3), ("gqa4_uniform", 32, 8, 32, 8192, 7)])
+def test_uniform_gqa_workloads_in_bench_configuration(lib, name, Hq, Hkv, B, ctx, seed):
+    """The two uniform GQA workloads the benchmark times (GQA-8 64 x 4096,
+    and GQA-4 32 x 8192 on the mma tiles), with its inputs and split count."""
+    p = workloads.make_problem(name, Hq, Hkv, 128, 16, np.full(B, ctx), 1, B * ctx // 16,
+                               workloads.BASE_SEED + seed, device="cuda")
+    out, lse, S = _decode(lib, p, num_splits=-1)
+    _check(p, out, lse, seqs=[0, B // 2, B - 1], what=f"{name} S={S}")
 
 
 @pytest.mark.parametrize("S", [0, -1, 1, 8, 32, 128])
