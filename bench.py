@@ -94,7 +94,7 @@ for _b in (1, 8, 32, 64):
 # kernel sources it was taken with: when the sources hash differently, the
 # bench reports traffic as null.
 MEASURED_TRAFFIC = {
-    "decode_64x8192": {"src": "c083c8138855a550", "bytes": 2149280512, "num_splits": 2},
+    "decode_64x8192": {"src": "86eac2e7161a8320", "bytes": 2149813120, "num_splits": 2},
 }
 
 

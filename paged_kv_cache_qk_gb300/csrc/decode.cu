@@ -27,10 +27,11 @@
 // consume, one per kv head, every q row that reads their kv head
 // (rows = q_len * group):
 //   * rows <= 2 ("simt", GQA-2 and multi-head decode): 8 lanes per key, 4
-//     keys per warp instruction; each lane holds 16 of the 128 dims, the q.k
-//     dot is a 3-step xor-shuffle reduction; every 8-lane key group keeps
-//     its own online softmax and the four groups are merged by shuffles at
-//     the end of a segment.
+//     keys per warp instruction; each lane holds 16 of the 128 dims, its
+//     part of q.k and of the P V update in packed fp32x2 FMAs (two dims per
+//     instruction), the q.k dot finished by a 3-step xor-shuffle reduction;
+//     every 8-lane key group keeps its own online softmax and the four groups
+//     are merged by shuffles at the end of a segment.
 //   * rows 3..16 ("tc", GQA-4 and GQA-8 decode, verify): the 16 padded rows
 //     x 16 keys score tile and the 16 rows x 128 dims output tile are
 //     mma.sync m16n8k16 bf16 contractions fed by ldmatrix from the swizzled
@@ -440,9 +441,14 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
         const int n = key0 + row;
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
-          float d = 0.f;
+          // 16 products in 8 packed fp32x2 FMAs (even and odd dims), then one add
+          uint64_t d2 = pack2(0.f, 0.f);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) d = fmaf(qf[rr][j], kf[j], d);
+          for (int j = 0; j < 8; ++j)
+            d2 = fma2(pack2(qf[rr][2 * j], qf[rr][2 * j + 1]), pack2(kf[2 * j], kf[2 * j + 1]), d2);
+          float d0, d1;
+          unpack2(d2, d0, d1);
+          float d = d0 + d1;
           d += __shfl_xor_sync(0xffffffffu, d, 4);
           d += __shfl_xor_sync(0xffffffffu, d, 2);
           d += __shfl_xor_sync(0xffffffffu, d, 1);
@@ -467,8 +473,12 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
           ls += pr[rr][q4];
         }
         l[rr] = ls;
+        const uint64_t alpha2 = pack2(alpha, alpha);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[rr][j] *= alpha;
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t a2 = mul2(pack2(acc[rr][2 * j], acc[rr][2 * j + 1]), alpha2);
+          unpack2(a2, acc[rr][2 * j], acc[rr][2 * j + 1]);
+        }
       }
 
 #pragma unroll
@@ -480,9 +490,15 @@ __device__ void consume_simt(const DecodeArgs& a, const Plan* plan, const uint8_
         unpack8(v0, vf);
         unpack8(v1, vf + 8);
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr)
+        for (int rr = 0; rr < R; ++rr) {
+          const uint64_t p2 = pack2(pr[rr][q4], pr[rr][q4]);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[rr][j] = fmaf(pr[rr][q4], vf[j], acc[rr][j]);
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t a2 = fma2(p2, pack2(vf[2 * j], vf[2 * j + 1]),
+                                     pack2(acc[rr][2 * j], acc[rr][2 * j + 1]));
+            unpack2(a2, acc[rr][2 * j], acc[rr][2 * j + 1]);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -673,12 +689,14 @@ __device__ void consume_tc(const DecodeArgs& a, const Plan* plan, const uint8_t*
       }
       lA = lA * alA + (sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]);
       lB = lB * alB + (sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]);
+      // rescale O in packed fp32 pairs (elements 0, 1: row A; 2, 3: row B)
+      const uint64_t alA2 = pack2(alA, alA), alB2 = pack2(alB, alB);
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        o[nt][0] *= alA;
-        o[nt][1] *= alA;
-        o[nt][2] *= alB;
-        o[nt][3] *= alB;
+        const uint64_t ta = mul2(pack2(o[nt][0], o[nt][1]), alA2);
+        const uint64_t tb = mul2(pack2(o[nt][2], o[nt][3]), alB2);
+        unpack2(ta, o[nt][0], o[nt][1]);
+        unpack2(tb, o[nt][2], o[nt][3]);
       }
       uint32_t pa[4];
       pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
