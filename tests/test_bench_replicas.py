@@ -80,3 +80,9 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, lines
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["n_gpus"] == 2
+    # the reference arm's line carries the contract's keys, on the product's metric
+    assert rec["metric"] == bench.METRIC and rec["unit"] == "GB/s"
+    assert rec["higher_is_better"] is True and rec["scaling"] == "weak"
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"]
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["value"] == rec["value"]
