@@ -34,6 +34,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -448,9 +449,8 @@ def main():
 
     # the clock sampler starts (and settles) before the warm-up, so that the
     # warm-up, not an idle pause, is what directly precedes the timed steps
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                          else f"/tmp/pkvqk_bench_clocks_r{rank}.csv")
+    clocks = ClockSampler(local, os.path.join(tempfile.gettempdir(),
+                                              f"pkvqk_bench_clocks_r{rank}.csv"))
     time.sleep(0.3)
 
     for _ in range(args.warmup):
