@@ -23,8 +23,10 @@
  * Conventions shared by every call
  * --------------------------------
  * - Every buffer is owned by the caller; the library allocates no device
- *   memory and keeps no state beyond a per-thread error message and a cached
- *   per-device SM count.
+ *   memory and keeps no state beyond a per-thread error message, facts it
+ *   caches per device (the SM count; each kernel's shared-memory limit, set
+ *   once), the rotary sin/cos knot table it builds once on the host, and the
+ *   fixed scratch of pkvqk_paged_decode_static_ws (below).
  * - Pointers marked "device" must be device (or managed) memory of the
  *   current device; they are checked with cudaPointerGetAttributes and a
  *   host pointer is rejected with PKVQK_ERR_POINTER_RESIDENCY.
