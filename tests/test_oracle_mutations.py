@@ -8,10 +8,8 @@ the pins that should notice it; every one must fail.  The mistakes live only
 in this test, on the CPU.
 """
 
-import math
 
 import numpy as np
-import pytest
 
 import oracle.reference as ref
 from tests import test_oracle_attention as ta
