@@ -255,13 +255,19 @@ PKVQK_API pkvqk_status pkvqk_paged_decode_partials(
  * library (pkvqk_static_workspace_capacity()), held on every GPU that loads
  * the library until the process exits.  A call whose partials need more
  * (pkvqk_decode_workspace_bytes for its split count) returns
- * PKVQK_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The call allocates
- * nothing.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls on a device share the one array and
- * it keeps the last call's partials: calls that can overlap on the GPU
- * (different streams, no ordering between them) race and corrupt each
- * other's results.  Nothing in it needs to start at zero.
+ * PKVQK_ERR_WORKSPACE_TOO_SMALL and launches nothing; so does a
+ * num_splits == 0 call whose chosen split count needs more.  Arguments that
+ * pkvqk_paged_decode rejects are rejected the same way here.  The call
+ * allocates nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it for
+ * the CUDA context current at that time; a later call under another context
+ * of the device (a driver context made current by the caller, or the primary
+ * context re-created after cudaDeviceReset) looks it up again.  Make the
+ * first call in each context before any stream capture.  All calls on a
+ * device share the one array and it keeps the last call's partials: calls
+ * that can overlap on the GPU (different streams, no ordering between them)
+ * race and corrupt each other's results.  Nothing in it needs to start at
+ * zero.
  */
 PKVQK_API pkvqk_status pkvqk_paged_decode_static_ws(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,

@@ -163,3 +163,23 @@ def test_split_heuristic_above_16_rows_is_the_tensor_core_choice(lib):
         S = lib.choose_num_splits(B, hkv, rows, L, B * L // 2, 16, 152)
         assert S == lib.choose_prefill_splits(B, hkv, rows, 1, L, 152)
         assert S >= 1
+
+
+def test_static_ws_reports_argument_errors_before_its_capacity(lib):
+    # arguments pkvqk_paged_decode rejects come back as argument errors from
+    # the static-workspace entry point too, even where their partials would
+    # also overflow its fixed array (16 MiB)
+    lay = _layout(lib)
+
+    def call(B=4, q_len=1, Hq=16, S=1, lay=lay):
+        return lib.pkvqk_paged_decode_static_ws(FAKE, 2048, 128, FAKE, FAKE, ctypes.byref(lay),
+                                                FAKE, 16, FAKE, B, q_len, Hq, S, 256, 0.0, FAKE,
+                                                None, None, None)
+    assert call(B=4096, S=300) == lib.PKVQK_ERR_INVALID_ARG            # num_splits > 256
+    assert "num_splits" in lib.pkvqk_last_error().decode()
+    assert call(B=4096, q_len=17, S=200) == lib.PKVQK_ERR_INVALID_ARG  # q_len > 16
+    assert call(B=4096, Hq=12, S=200) == lib.PKVQK_ERR_INVALID_ARG     # Hq % Hkv != 0
+    assert call(lay=_layout(lib, d=64)) == lib.PKVQK_ERR_UNSUPPORTED
+    # a valid call whose partials do not fit is refused before any launch
+    assert call(B=4096, S=200) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
+    assert call(B=0, S=4) == lib.PKVQK_OK
