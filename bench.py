@@ -3,8 +3,9 @@
 
 One step = the whole hot path over one batch: fused per-head RMSNorm + neox
 RoPE on q/k with the k/v append (pkvqk_norm_rope_append), split-KV paged
-decode attention (pkvqk_paged_decode / _partials) and, when the split count
-is above 1, the LSE combine (pkvqk_lse_combine) — all through the C ABI.
+decode attention (pkvqk_paged_decode) and, when the split count is above 1
+or the schedule is the balanced one, the LSE combine kernel it launches — all
+through the C ABI.
 
 Default workload: Qwen3-0.6B decode, 16 q / 8 kv heads, head_dim 128, bf16,
 block_size 16, batch 64 x context 8192, shuffled block ids (2.15 GB of K/V
@@ -18,11 +19,23 @@ around each call (the per-call durations of `roofline`); the `e2e` pass adds
 every step's host-to-device input copy and device-to-host output copy,
 pipelined on their own streams.
 
+The same line carries `sweep`: every decode configuration of the batch x
+context study measured the same way (the 12 batch x context points of the
+Qwen3-0.6B decode, the 8 x 32768 long context at the heuristic split count
+and at 1, 8, 32 and 128 splits, the GQA-8 serving batch of mixed lengths,
+the 32 x 5-token speculative verify, and two uniform GQA shapes), each with
+its own clocks; and `cpu_baseline`: the fp64 oracle timed on the host cores,
+on one core and on all cores (a process pool over sequences, or over
+(sequence, kv head) units for a batch smaller than the pool),
+for the largest batch x context point, the long context, the GQA-8 batch and
+the verify step.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle as reference arm
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
-replica (replicas only: the step has no exchange between GPUs).
+replica (replicas only: the step has no exchange between GPUs); the sweep and
+the CPU baseline run at N = 1 only.
 """
 
 from __future__ import annotations
@@ -87,14 +100,27 @@ for _b in (1, 8, 32, 64):
         WORKLOADS.setdefault(f"decode_{_b}x{_c}", ("decode_uniform", {"batch": _b, "ctx": _c},
                              f"Qwen3-0.6B decode 16q/8kv D128 bf16 bs16, batch {_b} x ctx {_c}"))
 
+# The decode configurations of the batch x context study, each with the split
+# count it is timed at (-1: the library's heuristic, 0: balanced schedule).
+SWEEP = ([(f"decode_{b}x{c}", -1, "batch x context") for b in (1, 8, 32, 64)
+          for c in (512, 2048, 8192)]
+         + [("decode_long_8x32768", s, "long context") for s in (-1, 1, 8, 32, 128)]
+         + [("decode_gqa8_64", -1, "GQA-8 serving batch"),
+            ("verify_32x5", -1, "speculative verify"),
+            ("decode_gqa8_64x4096", -1, "GQA-8 uniform"),
+            ("decode_gqa4_32x8192", -1, "GQA-4 uniform")])
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode-kernel launch,
-# mean of two launches from the 1-pass ncu capture recorded in
-# profiles/paged_decode_kernel_decode_64x8192.md.  A capture describes the
+# The oracle's CPU timing covers these decode configurations.
+CPU_BASELINE_WORKLOADS = ("decode_64x8192", "decode_long_8x32768", "decode_gqa8_64",
+                          "verify_32x5")
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode-kernel launch
+# (1-pass ncu captures of the full-size workloads, mean over the captured
+# launches), keyed by workload and split count.  A capture describes the
 # kernel sources it was taken with: when the sources hash differently, the
 # bench reports traffic as null.
 MEASURED_TRAFFIC = {
-    "decode_64x8192": {"src": "86eac2e7161a8320", "bytes": 2149813120, "num_splits": 2},
+    ("decode_64x8192", 2): {"src": "86eac2e7161a8320", "bytes": 2149813120},
 }
 
 
@@ -108,6 +134,11 @@ def kernel_src_hash():
     return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
 
 
+def measured_traffic(workload, S):
+    rec = MEASURED_TRAFFIC.get((workload, S))
+    return rec["bytes"] if rec and rec["src"] == kernel_src_hash() else None
+
+
 def load_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -116,6 +147,21 @@ def load_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
         return float(d[key]), "measured"
     except Exception:
         return fallback, "fallback"
+
+
+def build_problem(name, device):
+    """The seeded synthetic inputs of a named workload."""
+    import numpy as np
+
+    from paged_kv_cache_qk_gb300 import workloads
+    builder, kw, _ = WORKLOADS[name]
+    if builder == "make_problem_uniform_gqa8":
+        return workloads.make_problem("gqa8_uniform", 32, 4, 128, 16, np.full(64, 4096), 1,
+                                      64 * 256, workloads.BASE_SEED + 3, device=device)
+    if builder == "make_problem_uniform_gqa4":
+        return workloads.make_problem("gqa4_uniform", 32, 8, 128, 16, np.full(32, 8192), 1,
+                                      32 * 512, workloads.BASE_SEED + 7, device=device)
+    return getattr(workloads, builder)(device=device, **kw)
 
 
 def attention_flops(p):
@@ -148,16 +194,18 @@ def step_bytes(p):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / throttle sampling while the timed regions run; the
+    samples carry timestamps, so any wall-clock window can be summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index, path):
         self.path = path
         self.proc = None
-        self.gpu = gpu_index
+        self.samples = []
         try:
             self.fh = open(path, "w")
             self.proc = subprocess.Popen(
@@ -169,73 +217,254 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], None, set()
+        import datetime
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx = float(parts[2])
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm, mx = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        if not sm:
+                active = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower() == "active"}
+                self.samples.append((t, sm, mx, active))
+
+    def window(self, t0, t1):
+        """Median SM clock, max clock and active throttle reasons between two
+        time.time() stamps (the nearest sample if none falls inside)."""
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        reasons = set()
+        for s in inside:
+            reasons |= s[3]
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
-def cpu_baseline_sample(seconds=10.0, max_seqs=64, ctx=8192, seed=2024):
-    """Time the fp64 oracle on sequences of the benchmark workload's shape.
+# --------------------------------------------------------------------------
+# The fp64 oracle on the host cores (cpu_baseline and the reference arm).
+# A decode workload splits into independent units: a sequence (the oracle
+# called as it stands on the one-sequence sub-problem), or, when the batch
+# has fewer sequences than workers, a (sequence, kv head) pair (the
+# sequence's q heads of that kv head over that kv head's cache).  All cores:
+# a spawn pool over the units, the inputs shared through POSIX shared memory.
+# --------------------------------------------------------------------------
 
-    Runs in this process with whatever threads numpy uses; called from a
-    child process pinned to one BLAS thread so the core count is known.
-    """
+_ORACLE_STATE = {}
+
+
+def _oracle_attach(spec):
+    """Pool initializer: map the shared input arrays."""
     import numpy as np
+    from multiprocessing import shared_memory
+    shms = []
+    for key, (shm_name, shape, dtype) in spec["arrays"].items():
+        shm = shared_memory.SharedMemory(name=shm_name)
+        shms.append(shm)
+        _ORACLE_STATE[key] = np.ndarray(shape, dtype=dtype, buffer=shm.buf)
+    _ORACLE_STATE["_shms"] = shms
+    _ORACLE_STATE["meta"] = spec["meta"]
 
+
+def _oracle_unit(unit, state=None):
+    """One unit of the fp64 oracle: sequence b over all its kv heads (g < 0),
+    or over kv head g alone."""
     import oracle
-    from paged_kv_cache_qk_gb300 import workloads
+    st = _ORACLE_STATE if state is None else state
+    m = st["meta"]
+    b, g = unit
+    G, T = m["G"], m["q_len"]
+    if g < 0:
+        q, kc, vc = st["q"][b:b + 1], st["kc"], st["vc"]
+    else:
+        q = st["q"][b:b + 1, :, g * G:(g + 1) * G, :]
+        kc, vc = st["kc"][:, :, g:g + 1, :], st["vc"][:, :, g:g + 1, :]
+    out, _ = oracle.paged_attention(q, kc, vc, st["bt"][b:b + 1], st["sl"][b:b + 1], m["bs"],
+                                    q_len=T)
+    return float(out[0, 0, 0, 0])
 
-    import torch
 
-    chunk = 8
-    p = workloads.decode_uniform(chunk, ctx, device="cpu", seed=seed)
-    q = p.q.view(torch.int16).numpy().view(np.uint16).reshape(chunk, 1, p.Hq, p.D)
-    kb = p.k_cache.view(torch.int16).numpy().view(np.uint16)
-    vb = p.v_cache.view(torch.int16).numpy().view(np.uint16)
-    done_seqs, done_bytes, elapsed = 0, 0, 0.0
-    while done_seqs < max_seqs and elapsed < seconds:
+class OracleWorkload:
+    """A decode workload's inputs as host arrays, cut into independent units
+    (whole sequences when the batch has at least one sequence per worker,
+    else (sequence, kv head) pairs), timed through the oracle on one core or
+    on a pool."""
+
+    def __init__(self, name, workers):
+        import numpy as np
+        import torch
+        self.name = name
+        p = build_problem(name, "cpu")
+        self.p = p
+
+        def u16(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        self.arrays = {
+            "q": u16(p.q).reshape(p.B, p.q_len, p.Hq, p.D),
+            "kc": u16(p.k_cache), "vc": u16(p.v_cache),
+            "bt": np.ascontiguousarray(p.block_tables_host),
+            "sl": np.ascontiguousarray(p.seq_lens_host.astype(np.int64)),
+        }
+        self.meta = {"G": p.Hq // p.Hkv, "q_len": p.q_len, "bs": p.block_size}
+        # longest first, so a pool finishes together
+        order = np.argsort(-p.seq_lens_host, kind="stable")
+        self.per_sequence = p.B >= workers
+        heads = [-1] if self.per_sequence else list(range(p.Hkv))
+        self.units = [(int(b), g) for b in order for g in heads]
+        self.unit_kind = "sequence" if self.per_sequence else "(sequence, kv head)"
+        decode_bytes = step_bytes(p)[0]
+        kv_total = int(p.seq_lens_host.sum()) * len(heads)
+        # a unit's share of the step's algorithmic bytes: its keys' share
+        self.unit_bytes = {(b, g): decode_bytes * int(p.seq_lens_host[b]) / kv_total
+                           for b, g in self.units}
+        self.step_bytes = decode_bytes
+        self.shms = []
+
+    def time_one_core(self, seconds):
+        """Units in order on this process (one BLAS thread expected) until
+        `seconds` have passed or the workload is done; returns a record."""
+        state = dict(self.arrays, meta=self.meta)
         t0 = time.perf_counter()
-        oracle.paged_attention(q, kb, vb, p.block_tables_host, p.seq_lens_host, p.block_size)
-        elapsed += time.perf_counter() - t0
-        done_seqs += chunk
-        done_bytes += step_bytes(p)[0]
-    return {"seqs": done_seqs, "ctx": ctx, "bytes": done_bytes, "seconds": elapsed}
+        done, nbytes = 0, 0.0
+        for u in self.units:
+            _oracle_unit(u, state)
+            done += 1
+            nbytes += self.unit_bytes[u]
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        return {"gbs": nbytes / dt / 1e9, "cores": 1, "seconds": dt, "units": done,
+                "units_total": len(self.units), "unit": self.unit_kind}
+
+    def _share(self):
+        from multiprocessing import shared_memory
+        import numpy as np
+        spec = {"arrays": {}, "meta": self.meta}
+        for key, a in self.arrays.items():
+            shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            self.shms.append(shm)
+            np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf)[...] = a
+            spec["arrays"][key] = (shm.name, a.shape, a.dtype.str)
+        return spec
+
+    def open_pool(self, workers):
+        import multiprocessing as mp
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        spec = self._share()
+        self.pool = mp.get_context("spawn").Pool(workers, initializer=_oracle_attach,
+                                                 initargs=(spec,))
+        self.workers = workers
+        # start every worker and map the arrays before anything is timed
+        self.pool.map(_oracle_unit, self.units[-workers:], chunksize=1)
+
+    def pass_all_cores(self):
+        """One whole pass of the workload over the pool; returns seconds."""
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_unit, self.units, chunksize=1)
+        return time.perf_counter() - t0
+
+    def time_all_cores(self, seconds, max_passes=20):
+        total, passes = 0.0, 0
+        while passes < max_passes and (passes == 0 or total < seconds):
+            total += self.pass_all_cores()
+            passes += 1
+        return {"gbs": passes * self.step_bytes / total / 1e9, "cores": self.workers,
+                "seconds": total, "passes": passes, "units_total": len(self.units),
+                "unit": self.unit_kind}
+
+    def close(self):
+        pool = getattr(self, "pool", None)
+        if pool is not None:
+            pool.close()
+            pool.join()
+            self.pool = None
+        for shm in self.shms:
+            shm.close()
+            shm.unlink()
+        self.shms = []
 
 
-def run_cpu_baseline_child(seconds, max_seqs, ctx):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_child(seconds):
+    """Time the oracle on each CPU-baseline workload, one core then all."""
+    res = {"nproc": os.cpu_count(), "cores_available": host_cores(), "workloads": {}}
+    for name in CPU_BASELINE_WORKLOADS:
+        w = OracleWorkload(name, res["cores_available"])
+        try:
+            one = w.time_one_core(seconds)
+            w.open_pool(res["cores_available"])
+            allc = w.time_all_cores(seconds)
+        finally:
+            w.close()
+        res["workloads"][name] = {"one_core": one, "all_cores": allc,
+                                  "description": WORKLOADS[name][2]}
+        del w
+    return res
+
+
+def run_cpu_baseline_child(seconds):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
-           "--cpu-seconds", str(seconds), "--cpu-max-seqs", str(max_seqs), "--cpu-ctx", str(ctx)]
-    r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, timeout=600)
+           "--cpu-seconds", str(seconds)]
+    r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr.decode(errors="replace")[-300:]}
     return json.loads(r.stdout.decode().strip().splitlines()[-1])
+
+
+def cpu_baseline_record(cb, headline):
+    """The JSON line's cpu_baseline object from the child's measurements."""
+    if "error" in cb:
+        return {"error": cb["error"]}
+    ws = cb["workloads"]
+    head = headline if headline in ws else CPU_BASELINE_WORKLOADS[0]
+    h = ws[head]
+    per = {}
+    for name, r in ws.items():
+        per[name] = {
+            "one_core_gbs": round(r["one_core"]["gbs"], 4),
+            "all_cores_gbs": round(r["all_cores"]["gbs"], 4),
+            "cores": r["all_cores"]["cores"],
+            "sample": (f"one core: {r['one_core']['units']} of {r['one_core']['units_total']} "
+                       f"{r['one_core']['unit']} units in {r['one_core']['seconds']:.1f} s; all cores: "
+                       f"{r['all_cores']['passes']} whole pass(es) in "
+                       f"{r['all_cores']['seconds']:.1f} s"),
+        }
+    return {
+        "value": round(h["all_cores"]["gbs"], 4), "unit": "GB/s",
+        "cores": h["all_cores"]["cores"], "kind": "oracle",
+        "sample": (f"{WORKLOADS[head][2]}: the fp64 numpy oracle over {h['all_cores']['unit']} "
+                   f"units, a spawn process pool of {h['all_cores']['cores']} workers with one "
+                   f"BLAS thread each, {h['all_cores']['passes']} whole pass(es) of the workload "
+                   f"in {h['all_cores']['seconds']:.1f} s"),
+        "one_core": {"value": round(h["one_core"]["gbs"], 4), "unit": "GB/s", "cores": 1,
+                     "sample": per[head]["sample"].split(";")[0]},
+        "nproc": cb["nproc"],
+        "workloads": per,
+    }
 
 
 def max_over_ranks(values, device):
@@ -266,10 +495,12 @@ def dist_env():
 def run_reference(args):
     """Reference arm: the fp64 CPU oracle timed on the host cores.
 
-    Decode workloads: the oracle over one sequence of the workload's context
-    per step (GB/s).  Multi-query (prefill) workloads: the oracle over the
-    last tokens of one sequence's chunk, each with its whole causal context,
-    per step (TFLOP/s, the same algorithmic flop count as the GPU arm)."""
+    Decode workloads: each step is one whole pass of the workload through the
+    oracle, its (sequence, kv head) units spread over a spawn pool of one
+    worker per host core (GB/s).  Multi-query (prefill) workloads: the oracle
+    over the last tokens of one sequence's chunk, each with its whole causal
+    context, per step (TFLOP/s, the same algorithmic flop count as the GPU
+    arm)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -279,14 +510,13 @@ def run_reference(args):
     import torch
 
     import oracle
-    from paged_kv_cache_qk_gb300 import workloads
 
     def u16(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
     if name in PREFILL_WORKLOADS:
         # one sequence of the workload, the last `tail` tokens of its chunk
-        p = getattr(workloads, builder)(device="cpu", **kw)
+        p = build_problem(name, "cpu")
         b = int(np.argmax(p.seq_lens_host))
         q_lens = p.q_lens_host if p.q_lens_host is not None else np.full(p.B, p.q_len)
         cu = np.concatenate([[0], np.cumsum(q_lens)])
@@ -303,26 +533,30 @@ def run_reference(args):
         sample = (f"sequence {b}: its last {tail} new tokens with {L - tail + 1}..{L} visible "
                   f"keys each ({p.Hq}q/{p.Hkv}kv, D128) per step; numpy default threads")
         metric, unit, scale = PREFILL_METRIC, "TFLOP/s", 1e12
-        work = flops
+        work, cores = flops, os.cpu_count()
+        closer = None
     else:
-        ctx = kw.get("ctx", 8192)
-        seqs_per_step = 1
-        p = workloads.decode_uniform(seqs_per_step, ctx, device="cpu", seed=4242)
-        rows = u16(p.q).reshape(seqs_per_step, 1, p.Hq, p.D)
-        kb, vb = u16(p.k_cache), u16(p.v_cache)
+        cores = host_cores()
+        w = OracleWorkload(name, cores)
+        w.open_pool(cores)
 
         def once():
-            oracle.paged_attention(rows, kb, vb, p.block_tables_host, p.seq_lens_host,
-                                   p.block_size)
-        sample = f"{seqs_per_step} sequence x ctx {ctx} (16q/8kv, D128) per step; numpy default threads"
+            w.pass_all_cores()
+        sample = (f"one whole pass of the workload per step: {len(w.units)} {w.unit_kind} "
+                  f"units over a spawn process pool of {cores} workers, one BLAS thread each")
         metric, unit, scale = METRIC, "GB/s", 1e9
-        work = step_bytes(p)[0]
-    for _ in range(args.warmup):
-        once()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        once()
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
+        work = w.step_bytes
+        closer = w.close
+    try:
+        for _ in range(args.warmup):
+            once()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            once()
+        dt = (time.perf_counter() - t0) / max(1, args.steps)
+    finally:
+        if closer is not None:
+            closer()
     rate = work / dt / scale
     line = {
         "impl": "reference", "metric": metric, "value": rate, "unit": unit,
@@ -330,12 +564,236 @@ def run_reference(args):
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": desc, "sample": sample},
-        "cpu_baseline": {"value": rate, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# --------------------------------------------------------------------------
+# The GPU arm
+# --------------------------------------------------------------------------
+
+class StepRunner:
+    """One workload on the GPU through the C ABI: its buffers, its split
+    count, one step (append + attention call), and the timed passes."""
+
+    def __init__(self, lib, name, p, S_arg, dev, stream, flush):
+        import torch
+        self.lib, self.name, self.p, self.dev, self.stream = lib, name, p, dev, stream
+        self.prefill = name in PREFILL_WORKLOADS
+        self.varlen = p.cu_seqlens is not None
+        rows_per_kv = p.q_len * p.Hq // p.Hkv
+        if self.prefill:
+            S = S_arg if S_arg >= 1 else lib.choose_prefill_splits(
+                p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
+            ws_bytes = lib.prefill_workspace_bytes(1, p.T, p.Hq, p.D, S)
+            self.launches_per_step = 2 + (1 if S > 1 else 0)
+        else:
+            S = S_arg if S_arg >= 0 else lib.choose_num_splits(
+                p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
+            ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
+            self.launches_per_step = 2 + (1 if S != 1 else 0)
+        self.S = S
+        self.ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if ws_bytes else None
+        self.out = (torch.empty(p.T, p.Hq, p.D, dtype=torch.bfloat16, device=dev) if self.varlen else
+                    torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev))
+        self.q = p.q.clone()
+        self.decode_bytes, self.append_bytes = step_bytes(p)
+        l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.l2_bytes = l2_bytes
+        self.big_inputs = self.decode_bytes > 4 * l2_bytes
+        self.flush = flush
+
+    def cold_l2(self):
+        # write 2x L2 (evicts every input line), then read another 2x L2 so
+        # the written lines go back to HBM here and not inside the next step
+        self.flush[0].zero_()
+        self.flush[1].max()
+
+    def decode_call(self, qq, bt, sl, cu=None, o=None):
+        p, lib, S, stream = self.p, self.lib, self.S, self.stream
+        o = self.out if o is None else o
+        if self.varlen:
+            lib.paged_prefill_varlen(qq, p.cu_seqlens if cu is None else cu, p.q_len,
+                                     p.k_cache, p.v_cache, bt, sl, o, num_splits=S,
+                                     max_seq_len_hint=p.max_seq_len, workspace=self.ws,
+                                     stream=stream)
+        elif self.prefill:
+            lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
+                              num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=self.ws,
+                              stream=stream)
+        else:
+            lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
+                             num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=self.ws,
+                             stream=stream)
+
+    def step(self, ev=None):
+        p, stream = self.p, self.stream
+        if ev is not None:
+            ev[0].record(stream)
+        self.lib.norm_rope_append(self.q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q,
+                                  p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        self.decode_call(self.q, p.block_tables, p.seq_lens)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def warm(self, W):
+        import torch
+        for _ in range(W):
+            if not self.big_inputs:
+                self.cold_l2()
+            self.step()
+        torch.cuda.synchronize()
+
+    def time_value(self, K):
+        """Pass 1, the step value: K steps as a caller issues them, with no
+        event between the calls of a step (an event recorded between two
+        kernels ends the programmatic-dependent overlap of the second one's
+        launch and prologue with the first one's tail).  Returns total ms."""
+        import torch
+        stream = self.stream
+        if self.big_inputs:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(K):
+                self.step()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1)
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K)]
+        for i in range(K):
+            self.cold_l2()
+            step_ev[i][0].record(stream)
+            self.step()
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in step_ev)
+
+    def time_calls(self, K):
+        """Pass 2, the per-call durations: the same K steps with an event
+        before and after each call on the launching stream."""
+        import torch
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+        for i in range(K):
+            if not self.big_inputs:
+                self.cold_l2()
+            self.step(evs[i])
+        torch.cuda.synchronize()
+        return ([e[0].elapsed_time(e[1]) for e in evs], [e[1].elapsed_time(e[2]) for e in evs])
+
+    def time_e2e(self, K):
+        """End to end: host (pinned) inputs in, host output back, every step,
+        pipelined as a serving loop runs it (step i's inputs go up on an
+        upload stream and its output comes back on a readback stream while
+        the compute stream works on the neighbouring steps; two input and two
+        output buffers alternate, events order every reuse).  Returns
+        (ms per step, h2d bytes per step, d2h bytes per step)."""
+        import torch
+        p, dev, stream, lib = self.p, self.dev, self.stream, self.lib
+        # the step's inputs packed into one pinned host buffer (16-byte
+        # aligned fields), one host->device copy, typed device views into it
+        names = ("q", "k", "v", "positions", "slot_mapping", "block_tables", "seq_lens")
+        if self.varlen:
+            names = names + ("cu_seqlens",)
+        fields, off = {}, 0
+        for n in names:
+            t = getattr(p, n)
+            nbytes = t.numel() * t.element_size()
+            fields[n] = (off, nbytes, t.dtype, tuple(t.shape))
+            off += (nbytes + 15) // 16 * 16
+        host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        for n, (o, nb, dt, shp) in fields.items():
+            src = getattr(p, n).contiguous().view(torch.uint8).reshape(-1).cpu()
+            host_buf[o:o + nb].copy_(src)
+        dev_bufs = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+        dev_ins = [{n: dev_bufs[k][o:o + nb].view(dt).view(shp)
+                    for n, (o, nb, dt, shp) in fields.items()} for k in range(2)]
+        outs = [self.out, torch.empty_like(self.out)]
+        host_outs = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+                     for _ in range(2)]
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read_back = [torch.cuda.Event() for _ in range(2)]
+        for ev in computed + read_back:
+            ev.record(stream)
+
+        def e2e_step(i):
+            k = i & 1
+            with torch.cuda.stream(up):
+                up.wait_event(computed[k])           # step i - 2 is done reading buffer k
+                dev_bufs[k].copy_(host_buf, non_blocking=True)
+                uploaded[k].record(up)
+            stream.wait_event(uploaded[k])
+            stream.wait_event(read_back[k])          # step i - 2's output has left outs[k]
+            d = dev_ins[k]
+            lib.norm_rope_append(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"],
+                                 p.gamma_q, p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache,
+                                 stream=stream)
+            self.decode_call(d["q"], d["block_tables"], d["seq_lens"], d.get("cu_seqlens"),
+                             outs[k])
+            computed[k].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[k])
+                host_outs[k].copy_(outs[k], non_blocking=True)
+                read_back[k].record(down)
+
+        for i in range(4):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            e2e_step(i)
+        for ev in read_back:
+            stream.wait_event(ev)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K, off, host_outs[0].numel() * host_outs[0].element_size()
+
+    def schedule(self):
+        if self.prefill:
+            return f"256-row CTA tiles (2 x 128, ping-pong) x split {self.S}"
+        return "balanced (one CTA per SM)" if self.S == 0 else f"split x{self.S}"
+
+
+def sweep_point(runner, steps, warmup, peak, clocks, group):
+    """One configuration of the sweep: the step and the decode call timed as
+    the headline is; returns its record."""
+    p = runner.p
+    t0 = time.time()
+    runner.warm(warmup)
+    total_ms = runner.time_value(steps)
+    _, dec = runner.time_calls(steps)
+    t1 = time.time()
+    ms = total_ms / steps
+    dec_ms = statistics.fmean(dec)
+    step_gbs = (runner.decode_bytes + runner.append_bytes) / (ms * 1e-3) / 1e9
+    dec_gbs = runner.decode_bytes / (dec_ms * 1e-3) / 1e9
+    clk = clocks.window(t0, t1) if clocks is not None else None
+    return {
+        "workload": runner.name, "group": group, "batch": p.B, "ctx_max": p.max_seq_len,
+        "total_tokens": p.total_tokens, "q_len": p.q_len, "heads_q": p.Hq, "heads_kv": p.Hkv,
+        "num_splits": runner.S, "schedule": runner.schedule(), "steps": steps,
+        "ms_per_step": round(ms, 5), "step_gbs": round(step_gbs, 1),
+        "pct_of_nominal_8tbs": round(100.0 * step_gbs / NOMINAL_HBM_GBS, 2),
+        "decode_ms": round(dec_ms, 5), "decode_gbs": round(dec_gbs, 1),
+        "frac": round(dec_gbs / peak, 4),
+        "seq_steps_per_s": round(p.B / (ms * 1e-3), 1),
+        "algorithmic_bytes_per_launch": runner.decode_bytes,
+        "traffic": measured_traffic(runner.name, runner.S),
+        "l2": "inputs > 4x L2" if runner.big_inputs else "cold clean L2 before every step",
+        "sm_mhz": clk["sm_mhz"] if clk else None,
+        "clock_reasons": clk["reasons"] if clk else None,
+    }
 
 
 def main():
@@ -348,25 +806,26 @@ def main():
     ap.add_argument("--num-splits", type=int, default=-1,
                     help="0: balanced persistent schedule; -1: split heuristic; >0: fixed splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--cpu-max-seqs", type=int, default=4096)
-    ap.add_argument("--cpu-ctx", type=int, default=8192)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--sweep-only", default="",
+                    help="comma-separated workload names: restrict the sweep to them")
+    ap.add_argument("--cpu-seconds", type=float, default=3.0,
+                    help="oracle seconds per workload and core setting in cpu_baseline")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
 
     if args.cpu_baseline_child:
-        print(json.dumps(cpu_baseline_sample(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)))
+        print(json.dumps(cpu_baseline_child(args.cpu_seconds)))
         return 0
     if args.impl == "reference":
         return run_reference(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
-    import numpy as np
     import torch
 
     from paged_kv_cache_qk_gb300 import binding as lib
-    from paged_kv_cache_qk_gb300 import workloads
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -375,215 +834,45 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    builder, kw, desc = WORKLOADS[args.workload]
-    if builder == "make_problem_uniform_gqa8":
-        import numpy as _np
-        p = workloads.make_problem("gqa8_uniform", 32, 4, 128, 16, _np.full(64, 4096), 1,
-                                   64 * 256, workloads.BASE_SEED + 3, device=dev)
-    elif builder == "make_problem_uniform_gqa4":
-        import numpy as _np
-        p = workloads.make_problem("gqa4_uniform", 32, 8, 128, 16, _np.full(32, 8192), 1,
-                                   32 * 512, workloads.BASE_SEED + 7, device=dev)
-    else:
-        p = getattr(workloads, builder)(device=dev, **kw)
-    decode_bytes, append_bytes = step_bytes(p)
-    rows_per_kv = p.q_len * p.Hq // p.Hkv
-    prefill = args.workload in PREFILL_WORKLOADS
-    if prefill:
-        S = args.num_splits if args.num_splits >= 1 else lib.choose_prefill_splits(
-            p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
-        ws_bytes = lib.prefill_workspace_bytes(1, p.T, p.Hq, p.D, S)
-    else:
-        S = args.num_splits if args.num_splits >= 0 else lib.choose_num_splits(
-            p.B, p.Hkv, rows_per_kv, p.max_seq_len, p.total_tokens, p.block_size)
-        ws_bytes = lib.decode_workspace_bytes(p.B, p.q_len, p.Hq, p.D, S)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if ws_bytes else None
-    varlen = p.cu_seqlens is not None
-    out = (torch.empty(p.T, p.Hq, p.D, dtype=torch.bfloat16, device=dev) if varlen else
-           torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device=dev))
-    q = p.q.clone()
     stream = torch.cuda.current_stream()
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    big_inputs = decode_bytes > 4 * l2_bytes
-    flush = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
-    flush_clean = None if big_inputs else torch.empty(2 * l2_bytes, dtype=torch.uint8,
-                                                      device=dev)
+    flush = (torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev),
+             torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev))
 
-    def cold_l2():
-        # write 2x L2 (evicts every input line), then read another 2x L2 so
-        # the written lines go back to HBM here and not inside the next step
-        flush.zero_()
-        flush_clean.max()
-
-    def decode_call(qq, bt, sl, cu=None, o=None):
-        o = out if o is None else o
-        if varlen:
-            lib.paged_prefill_varlen(qq, p.cu_seqlens if cu is None else cu, p.q_len,
-                                     p.k_cache, p.v_cache, bt, sl, o, num_splits=S,
-                                     max_seq_len_hint=p.max_seq_len, workspace=ws, stream=stream)
-        elif prefill:
-            lib.paged_prefill(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
-                              num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
-                              stream=stream)
-        else:
-            lib.paged_decode(qq, p.k_cache, p.v_cache, bt, sl, o, q_len=p.q_len,
-                             num_splits=S, max_seq_len_hint=p.max_seq_len, workspace=ws,
-                             stream=stream)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        lib.norm_rope_append(q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q, p.gamma_k,
-                             p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        decode_call(q, p.block_tables, p.seq_lens)
-        if ev is not None:
-            ev[2].record(stream)
-
-    if prefill:   # append, prefill (+ lse combine when split)
-        launches_per_step = 2 + (1 if S > 1 else 0)
-    else:         # append, decode (+ the combine of the split or balanced partials)
-        launches_per_step = 2 + (1 if S != 1 else 0)
+    desc = WORKLOADS[args.workload][2]
+    p = build_problem(args.workload, dev)
+    run = StepRunner(lib, args.workload, p, args.num_splits, dev, stream, flush)
+    S = run.S
 
     # the clock sampler starts (and settles) before the warm-up, so that the
     # warm-up, not an idle pause, is what directly precedes the timed steps
     clocks = ClockSampler(local, os.path.join(tempfile.gettempdir(),
                                               f"pkvqk_bench_clocks_r{rank}.csv"))
     time.sleep(0.3)
-
-    for _ in range(args.warmup):
-        if not big_inputs:
-            cold_l2()
-        step()
-    torch.cuda.synchronize()
+    t_head0 = time.time()
+    run.warm(args.warmup)
     if world > 1:
         torch.distributed.barrier()
-
     K = args.steps
-    # Pass 1, the step value: K steps as a caller issues them, with no event
-    # between the calls of a step (an event recorded between two kernels ends
-    # the programmatic-dependent overlap of the second one's launch and
-    # prologue with the first one's tail).
-    if big_inputs:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(K):
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        total_ms = t0.elapsed_time(t1)
-    else:
-        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(K)]
-        for i in range(K):
-            cold_l2()
-            step_ev[i][0].record(stream)
-            step()
-            step_ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    total_ms = run.time_value(K)
     if world > 1:
         torch.distributed.barrier()
-    # Pass 2, the per-call durations for the roofline: the same K steps with an
-    # event before and after each call on the launching stream.
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
-    for i in range(K):
-        if not big_inputs:
-            cold_l2()
-        step(evs[i])
-    torch.cuda.synchronize()
-    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    decode_ms = [e[1].elapsed_time(e[2]) for e in evs]
-
-    # end to end: host (pinned) inputs in, host output back, every step
-    # the step's inputs packed into one pinned host buffer (16-byte aligned
-    # fields), one host->device copy, typed device views into the copy
-    names = ("q", "k", "v", "positions", "slot_mapping", "block_tables", "seq_lens")
-    if varlen:
-        names = names + ("cu_seqlens",)
-    fields, off = {}, 0
-    for n in names:
-        t = getattr(p, n)
-        nbytes = t.numel() * t.element_size()
-        fields[n] = (off, nbytes, t.dtype, tuple(t.shape))
-        off += (nbytes + 15) // 16 * 16
-    host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(off, dtype=torch.uint8, device=dev)
-    dev_in = {}
-    for n, (o, nb, dt, shp) in fields.items():
-        src = getattr(p, n).contiguous().view(torch.uint8).reshape(-1).cpu()
-        host_buf[o:o + nb].copy_(src)
-        dev_in[n] = dev_buf[o:o + nb].view(dt).view(shp)
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = off
-    d2h = host_out.numel() * host_out.element_size()
+    append_ms, decode_ms = run.time_calls(K)
     K_e2e = max(3, min(K, 500))
-
-    # Pipelined as a serving loop runs it: step i's inputs go up on an upload
-    # stream and its output comes back on a readback stream while the compute
-    # stream works on the neighbouring steps; two input and two output buffers
-    # alternate, and events order every reuse.  Each step still moves its own
-    # inputs and output inside the timed region.
-    dev_bufs = [dev_buf, torch.empty_like(dev_buf)]
-    dev_ins = [dev_in, {n: dev_bufs[1][o:o + nb].view(dt).view(shp)
-                        for n, (o, nb, dt, shp) in fields.items()}]
-    outs = [out, torch.empty_like(out)]
-    host_outs = [host_out, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
-    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    uploaded = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    read_back = [torch.cuda.Event() for _ in range(2)]
-    for ev in computed + read_back:
-        ev.record(stream)
-
-    def e2e_step(i):
-        k = i & 1
-        with torch.cuda.stream(up):
-            up.wait_event(computed[k])           # step i - 2 is done reading buffer k
-            dev_bufs[k].copy_(host_buf, non_blocking=True)
-            uploaded[k].record(up)
-        stream.wait_event(uploaded[k])
-        stream.wait_event(read_back[k])          # step i - 2's output has left outs[k]
-        d = dev_ins[k]
-        lib.norm_rope_append(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"],
-                             p.gamma_q, p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache,
-                             stream=stream)
-        decode_call(d["q"], d["block_tables"], d["seq_lens"], d.get("cu_seqlens"), outs[k])
-        computed[k].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(computed[k])
-            host_outs[k].copy_(outs[k], non_blocking=True)
-            read_back[k].record(down)
-
-    for i in range(4):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(K_e2e):
-        e2e_step(i)
-    for ev in read_back:
-        stream.wait_event(ev)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K_e2e
-    clk = clocks.stop()
+    e2e_ms, h2d, d2h = run.time_e2e(K_e2e)
+    t_head1 = time.time()
 
     ms = total_ms / K
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
+    decode_bytes, append_bytes = run.decode_bytes, run.append_bytes
     bytes_step = decode_bytes + append_bytes
     value = aggregate_rate(world, bytes_step, ms) / 1e9
     e2e_value = aggregate_rate(world, bytes_step, e2e_ms) / 1e9
 
     peak, peak_kind = load_peaks()
-    rec = MEASURED_TRAFFIC.get(args.workload)
-    traffic = (rec["bytes"] if rec and rec["src"] == kernel_src_hash() and rec["num_splits"] == S
-               else None)
     dec_avg_ms = statistics.fmean(decode_ms)
     achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
+    prefill = run.prefill
 
     line = {
         "metric": METRIC,
@@ -603,9 +892,9 @@ def main():
             "batch": p.B, "ctx_max": p.max_seq_len, "total_tokens": p.total_tokens,
             "q_len": p.q_len, "heads_q": p.Hq, "heads_kv": p.Hkv, "head_dim": p.D,
             "block_size": p.block_size,
-            "schedule": "balanced (one CTA per SM)" if S == 0 else f"split x{S}",
+            "schedule": run.schedule(),
             "l2": ("inputs larger than L2: %.2f GB of K/V per step vs %d MB L2" %
-                   (decode_bytes / 1e9, l2_bytes >> 20)) if big_inputs else
+                   (decode_bytes / 1e9, l2_bytes >> 20)) if run.big_inputs else
                   "L2 flushed before every step (2x L2 written, then 2x L2 read so the "
                   "written lines are back in HBM before the step), excluded from timing",
             "parallelism": f"replicas x{world}",
@@ -615,7 +904,7 @@ def main():
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "copies": "pipelined: upload and readback streams, double-buffered"},
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * run.launches_per_step,
         "roofline": {
             "kernel": "pkvqk_paged_decode call: paged_decode_kernel"
                       + (" + balanced_combine_kernel" if S == 0 else
@@ -626,14 +915,14 @@ def main():
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic,
+            "traffic": measured_traffic(args.workload, S),
             "algorithmic_bytes_per_launch": decode_bytes,
             "avg_launch_ms": round(dec_avg_ms, 5),
             "timing": "second pass of the K steps, CUDA events around each call",
         },
-        "clocks": clk,
+        "clocks": None,
         "append_avg_ms": round(statistics.fmean(append_ms), 5),
-        "e2e_gpu_launches": K_e2e * launches_per_step,
+        "e2e_gpu_launches": K_e2e * run.launches_per_step,
     }
     if prefill:
         flops = attention_flops(p)
@@ -644,7 +933,6 @@ def main():
         line["unit"] = "TFLOP/s"
         line["e2e"]["value"] = round(aggregate_rate(world, flops, e2e_ms) / 1e12, 2)
         line["e2e"]["unit"] = "TFLOP/s"
-        line["config"]["schedule"] = f"256-row CTA tiles (2 x 128, ping-pong) x split {S}"
         line["config"]["flops_per_step"] = flops
         line["config"]["kv_bytes_per_step"] = decode_bytes
         del line["pct_of_nominal_8tbs"]
@@ -664,18 +952,40 @@ def main():
             "timing": "second pass of the K steps, CUDA events around each call",
             "hbm_gbs_of_kv": round(achieved, 2),
         }
+    del run, p
+
+    # the batch x context study, N = 1 only (a rank's sweep would hold the
+    # other GPUs idle meanwhile)
+    sweep = None
+    if world == 1 and not args.no_sweep and not prefill:
+        only = {s for s in args.sweep_only.split(",") if s}
+        sweep = []
+        cache = {}
+        for name, S_arg, group in SWEEP:
+            if only and name not in only:
+                continue
+            if name not in cache:
+                cache.clear()
+                torch.cuda.empty_cache()
+                cache[name] = build_problem(name, dev)
+            r = StepRunner(lib, name, cache[name], S_arg, dev, stream, flush)
+            sweep.append(sweep_point(r, args.sweep_steps, 5, peak, clocks, group))
+            del r
+        cache.clear()
+        torch.cuda.empty_cache()
+    clocks.stop()
+    line["clocks"] = clocks.window(t_head0, t_head1)
+    if sweep is not None:
+        line["sweep"] = sweep
+        line["sweep_note"] = ("every decode configuration timed as the headline: step = append "
+                              "+ decode call, value pass without events inside a step, decode_ms "
+                              "from a second pass with events around each call; frac = decode "
+                              "GB/s / measured HBM copy GB/s; traffic = 1-pass ncu DRAM bytes "
+                              "of one decode launch where captured on the current sources")
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not prefill:
-        cb = run_cpu_baseline_child(args.cpu_seconds, args.cpu_max_seqs, args.cpu_ctx)
-        if "error" in cb:
-            line["cpu_baseline"] = {"error": cb["error"]}
-        else:
-            line["cpu_baseline"] = {
-                "value": round(cb["bytes"] / cb["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
-                "kind": "oracle",
-                "sample": f"{cb['seqs']} sequence-passes (8 seqs re-run) x ctx {cb['ctx']} of the "
-                          f"16q/8kv D128 decode workload, fp64 numpy oracle, 1 BLAS thread, "
-                          f"{cb['seconds']:.1f} s",
-            }
+        cb = run_cpu_baseline_child(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_record(cb, args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
