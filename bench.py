@@ -765,7 +765,7 @@ class StepRunner:
         return "balanced (one CTA per SM)" if self.S == 0 else f"split x{self.S}"
 
 
-def sweep_point(runner, steps, warmup, peak, clocks, group):
+def sweep_point(runner, steps, warmup, peak, group):
     """One configuration of the sweep: the step and the decode call timed as
     the headline is; returns its record."""
     p = runner.p
@@ -778,7 +778,6 @@ def sweep_point(runner, steps, warmup, peak, clocks, group):
     dec_ms = statistics.fmean(dec)
     step_gbs = (runner.decode_bytes + runner.append_bytes) / (ms * 1e-3) / 1e9
     dec_gbs = runner.decode_bytes / (dec_ms * 1e-3) / 1e9
-    clk = clocks.window(t0, t1) if clocks is not None else None
     return {
         "workload": runner.name, "group": group, "batch": p.B, "ctx_max": p.max_seq_len,
         "total_tokens": p.total_tokens, "q_len": p.q_len, "heads_q": p.Hq, "heads_kv": p.Hkv,
@@ -791,8 +790,7 @@ def sweep_point(runner, steps, warmup, peak, clocks, group):
         "algorithmic_bytes_per_launch": runner.decode_bytes,
         "traffic": measured_traffic(runner.name, runner.S),
         "l2": "inputs > 4x L2" if runner.big_inputs else "cold clean L2 before every step",
-        "sm_mhz": clk["sm_mhz"] if clk else None,
-        "clock_reasons": clk["reasons"] if clk else None,
+        "window": (t0, t1),        # replaced by the clocks seen in it once sampling stops
     }
 
 
@@ -969,13 +967,17 @@ def main():
                 torch.cuda.empty_cache()
                 cache[name] = build_problem(name, dev)
             r = StepRunner(lib, name, cache[name], S_arg, dev, stream, flush)
-            sweep.append(sweep_point(r, args.sweep_steps, 5, peak, clocks, group))
+            sweep.append(sweep_point(r, args.sweep_steps, 5, peak, group))
             del r
         cache.clear()
         torch.cuda.empty_cache()
     clocks.stop()
     line["clocks"] = clocks.window(t_head0, t_head1)
     if sweep is not None:
+        for rec in sweep:
+            clk = clocks.window(*rec.pop("window"))
+            rec["sm_mhz"] = clk["sm_mhz"] if clk else None
+            rec["clock_reasons"] = clk["reasons"] if clk else None
         line["sweep"] = sweep
         line["sweep_note"] = ("every decode configuration timed as the headline: step = append "
                               "+ decode call, value pass without events inside a step, decode_ms "
