@@ -115,12 +115,33 @@ CPU_BASELINE_WORKLOADS = ("decode_64x8192", "decode_long_8x32768", "decode_gqa8_
                           "verify_32x5")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode-kernel launch
-# (1-pass ncu captures of the full-size workloads, mean over the captured
-# launches), keyed by workload and split count.  A capture describes the
-# kernel sources it was taken with: when the sources hash differently, the
-# bench reports traffic as null.
+# (1-pass ncu captures of the full-size workloads, mean of two launches after
+# three warm-up steps), keyed by workload and split count (0: balanced).  A
+# capture describes the kernel sources it was taken with: when the sources
+# hash differently, the bench reports traffic as null.
+SRC_R1 = "86eac2e7161a8320"
 MEASURED_TRAFFIC = {
-    ("decode_64x8192", 2): {"src": "86eac2e7161a8320", "bytes": 2149813120},
+    ("decode_1x2048", 32): {"src": SRC_R1, "bytes": 8467968},
+    ("decode_1x512", 8): {"src": SRC_R1, "bytes": 2176128},
+    ("decode_1x8192", 64): {"src": SRC_R1, "bytes": 33635456},
+    ("decode_32x2048", 4): {"src": SRC_R1, "bytes": 270167424},
+    ("decode_32x512", 4): {"src": SRC_R1, "bytes": 67439488},
+    ("decode_32x8192", 4): {"src": SRC_R1, "bytes": 1075467264},
+    ("decode_64x2048", 2): {"src": SRC_R1, "bytes": 539003264},
+    ("decode_64x512", 2): {"src": SRC_R1, "bytes": 135935616},
+    ("decode_64x8192", 2): {"src": SRC_R1, "bytes": 2149567232},
+    ("decode_8x2048", 16): {"src": SRC_R1, "bytes": 67333248},
+    ("decode_8x512", 8): {"src": SRC_R1, "bytes": 16886016},
+    ("decode_8x8192", 16): {"src": SRC_R1, "bytes": 270138112},
+    ("decode_gqa4_32x8192", 4): {"src": SRC_R1, "bytes": 1075693952},
+    ("decode_gqa8_64x4096", 2): {"src": SRC_R1, "bytes": 539126400},
+    ("decode_gqa8_64", 0): {"src": SRC_R1, "bytes": 468566144},
+    ("decode_long_8x32768", 16): {"src": SRC_R1, "bytes": 1075467648},
+    ("decode_long_8x32768", 1): {"src": SRC_R1, "bytes": 1075839360},
+    ("decode_long_8x32768", 128): {"src": SRC_R1, "bytes": 1076142976},
+    ("decode_long_8x32768", 32): {"src": SRC_R1, "bytes": 1075754752},
+    ("decode_long_8x32768", 8): {"src": SRC_R1, "bytes": 1075975936},
+    ("verify_32x5", 0): {"src": SRC_R1, "bytes": 709335040},
 }
 
 

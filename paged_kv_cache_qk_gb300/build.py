@@ -22,8 +22,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkvqk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "norm_rope_append.cu", "decode.cu", "decode_tc5.cu", "combine.cu",
-           "decode_static_ws.cu", "prefill.cu"]
+SOURCES = ["api.cu", "norm_rope_append.cu", "decode.cu", "combine.cu", "decode_static_ws.cu",
+           "prefill.cu"]
 
 
 def nvcc() -> str:

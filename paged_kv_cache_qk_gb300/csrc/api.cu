@@ -142,29 +142,6 @@ pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_ca
   return PKVQK_OK;
 }
 
-// The same cache with dims (64 dims, slot, head, dim half, block): a box
-// (64, 16, heads_per_cta, 1, 1) lands as heads_per_cta x 16 rows of 128 B,
-// the row order the tcgen05 decode kernel's K operand needs.
-pkvqk_status encode_cache_map_heads(CUtensorMap* map, const void* base,
-                                    const pkvqk_cache_layout& L, int heads_per_cta) {
-  PKVQK_TRY(get_encoder());
-  cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(L.block_size),
-                        static_cast<cuuint64_t>(L.num_kv_heads), 2,
-                        static_cast<cuuint64_t>(L.num_blocks)};
-  cuuint64_t strides[4] = {static_cast<cuuint64_t>(L.slot_stride) * 2,
-                           static_cast<cuuint64_t>(L.head_stride) * 2, 128,
-                           static_cast<cuuint64_t>(L.block_stride) * 2};
-  cuuint32_t box[5] = {64, 16, static_cast<cuuint32_t>(heads_per_cta), 1, 1};
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(PKVQK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
-  return PKVQK_OK;
-}
-
 // ---------------------------------------------------------------- SM count
 
 int sm_count_current() {
@@ -298,13 +275,8 @@ pkvqk_status run_decode(const DecodeCall& c) {
   if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
 
   CUtensorMap kmap, vmap;
-  if (plan.tc5) {
-    PKVQK_TRY(encode_cache_map_heads(&kmap, c.k_cache, L, plan.heads_per_cta));
-    PKVQK_TRY(encode_cache_map_heads(&vmap, c.v_cache, L, plan.heads_per_cta));
-  } else {
-    PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta, plan.tile_keys));
-    PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta, plan.tile_keys));
-  }
+  PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, plan.heads_per_cta, plan.tile_keys));
+  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, plan.heads_per_cta, plan.tile_keys));
 
   const int hint_pages = (hint + L.block_size - 1) / L.block_size;
   pkvqk::DecodeArgs a;

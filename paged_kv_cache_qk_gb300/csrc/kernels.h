@@ -60,7 +60,6 @@ struct DecodeArgs {
 struct DecodePlan {
   int heads_per_cta;   // kv heads handled by one CTA (divides num_kv_heads)
   bool tensor_core;    // mma tiles (rows per kv head > 2) vs CUDA-core dots
-  bool tc5;            // the tcgen05 swapped-operand kernel instead of the mma tiles
   int rows;            // q_len * group
   int tile_keys;       // keys per TMA tile (8 or 16)
   int ctas_per_sm;     // resident CTAs per SM the shared-memory ring allows
@@ -72,13 +71,6 @@ DecodePlan plan_decode(int num_kv_heads, int rows);
 cudaError_t launch_paged_decode(const DecodePlan& plan, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const DecodeArgs& a, int grid_ctas,
                                 cudaStream_t stream);
-
-// The tcgen05 kernel (decode_tc5.cu) for 3..16 rows per kv head and 4 or 8
-// kv heads per CTA; its tensor maps have dims (64, slot, head, half, block)
-// and boxes (64, 16, heads_per_cta, 1, 1).
-cudaError_t launch_paged_decode_tc5(int heads_per_cta, const CUtensorMap& kmap,
-                                    const CUtensorMap& vmap, const DecodeArgs& a, int grid_ctas,
-                                    cudaStream_t stream);
 
 cudaError_t launch_lse_combine(const float* ws_o, const float* ws_lse, int rows, int num_splits,
                                __nv_bfloat16* out, float* lse_out, cudaStream_t stream);
