@@ -149,7 +149,7 @@ def kernel_src_hash():
     import hashlib
     csrc = os.path.join(ROOT, "paged_kv_cache_qk_gb300", "csrc")
     parts = []
-    for f in ("decode.cu", "device_common.cuh", "kernels.h"):
+    for f in ("decode.cu", "device_common.cuh", "kernels.h", "api.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             parts.append(hashlib.sha256(fh.read()).hexdigest())
     return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
@@ -783,7 +783,7 @@ class StepRunner:
     def schedule(self):
         if self.prefill:
             return f"256-row CTA tiles (2 x 128, ping-pong) x split {self.S}"
-        return "balanced (one CTA per SM)" if self.S == 0 else f"split x{self.S}"
+        return "balanced (persistent, 0.84 CTAs per SM)" if self.S == 0 else f"split x{self.S}"
 
 
 def sweep_point(runner, steps, warmup, peak, group):

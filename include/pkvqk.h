@@ -192,11 +192,12 @@ PKVQK_API size_t pkvqk_decode_workspace_bytes(int32_t batch, int32_t q_len,
  *   combine kernel that this call launches (as a programmatic dependent, so
  *   its launch overlaps the decode kernel's tail) merges them.
  *   pkvqk_choose_num_splits gives a host-side choice.
- * - num_splits == 0 (balanced): one CTA per SM; the pages of all (sequence,
- *   kv-head group) pairs are laid end to end and every CTA takes an equal
- *   contiguous share, crossing sequence boundaries; a sequence covered by one
- *   CTA is written directly, one cut across CTAs is merged by a combine
- *   kernel this call launches.  Balances any mix of lengths.
+ * - num_splits == 0 (balanced): a persistent grid of 0.84 CTAs per SM; the
+ *   pages of all (sequence, kv-head group) pairs are laid end to end and
+ *   every CTA takes an equal contiguous share, crossing sequence boundaries;
+ *   a sequence covered by one CTA is written directly, one cut across CTAs is
+ *   merged by a combine kernel this call launches.  Balances any mix of
+ *   lengths.
  *
  *   q             device bf16, element (b*q_len + t, h, d) at
  *                 q[(b*q_len + t)*q_stride_t + h*q_stride_h + d]

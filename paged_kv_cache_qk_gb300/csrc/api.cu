@@ -242,7 +242,11 @@ pkvqk_status run_decode(const DecodeCall& c) {
   const int S = c.num_splits;                   // 0: balanced schedule
   const pkvqk::DecodePlan plan = pkvqk::plan_decode(L.num_kv_heads, rows);
   const int64_t nrows = static_cast<int64_t>(c.batch) * c.q_len * c.num_q_heads;
-  const int grid_ctas = sm_count_current();
+  // balanced schedule: 0.84 CTAs per SM, the share the split heuristic also
+  // keeps in flight (measured on GB300 against one CTA per SM: decode call
+  // GQA-8 mixed batch 86.7 -> 83.9 us, verify 32 x 5 116.2 -> 113.7 us,
+  // 64 x 8192 315.7 -> 311.9 us; 112-144 CTAs within 1 %)
+  const int grid_ctas = std::max(1, static_cast<int>(std::lround(0.84 * sm_count_current())));
   const int groups = L.num_kv_heads / plan.heads_per_cta;
   const int64_t units = static_cast<int64_t>(c.batch) * groups;
   const int64_t rows_per_unit = static_cast<int64_t>(c.q_len) * plan.heads_per_cta * group;

@@ -13,7 +13,7 @@
 //   * split   (num_splits >= 1): grid (S, head groups, batch), one segment
 //     per CTA: split j of the sequence (chunk_pages pages per split, the last
 //     split takes the rest);
-//   * balanced (num_splits == 0): a persistent grid of one CTA per SM; the
+//   * balanced (num_splits == 0): a persistent grid (0.84 CTAs per SM); the
 //     pages of all (head group, sequence) units are laid end to end and CTA c
 //     takes pages [c*TP/G, (c+1)*TP/G) of that list (G = min(grid, TP)), crossing sequence
 //     boundaries without refilling its pipeline.  A unit that one CTA covers
