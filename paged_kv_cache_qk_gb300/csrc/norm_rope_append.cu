@@ -38,6 +38,12 @@ namespace {
 constexpr int kMaxThreads = 512;
 constexpr int kHoist = 4;            // vectors per half-warp whose loads go first
 constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
+// Narrow CTAs of at most kManyThreads threads, kManyMinBlocks of them per SM:
+// the compiler then keeps a thread at 80 registers, 8 tokens per SM (measured
+// on GB300, 8192 tokens: 6 per SM at 96 registers 55.4 us, 8 at 80 49.6 us,
+// 10 at 64 registers with spills 53.4 us).
+constexpr int kManyThreads = 96;
+constexpr int kManyMinBlocks = 8;
 
 struct Loaded {
   uint4 x, v;
@@ -116,7 +122,8 @@ __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t
   }
 }
 
-__global__ void __launch_bounds__(kMaxThreads)
+template <int kThreadsBound, int kMinBlocks>
+__global__ void __launch_bounds__(kThreadsBound, kMinBlocks)
 norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   __shared__ float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
   __shared__ float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
@@ -197,10 +204,15 @@ cudaError_t launch_norm_rope_append(const NormRopeAppendArgs& a, cudaStream_t st
   // few tokens: one half-warp per head vector; many: up to kHoist vectors per
   // half-warp; at least 2 warps (one angle per lane of warps 0 and 1)
   const int num_vec = a.num_q_heads + a.num_kv_heads;
-  const int per_half_warp = a.num_tokens >= kManyTokens ? kHoist : 1;
+  const bool many = a.num_tokens >= kManyTokens;
+  const int per_half_warp = many ? kHoist : 1;
   int warps = (num_vec + 2 * per_half_warp - 1) / (2 * per_half_warp);
   warps = warps < 2 ? 2 : (warps > kMaxThreads / 32 ? kMaxThreads / 32 : warps);
-  return launch_pdl(norm_rope_append_kernel, dim3(a.num_tokens), dim3(warps * 32), 0, stream, a);
+  if (many && warps * 32 <= kManyThreads)
+    return launch_pdl(norm_rope_append_kernel<kManyThreads, kManyMinBlocks>, dim3(a.num_tokens),
+                      dim3(warps * 32), 0, stream, a);
+  return launch_pdl(norm_rope_append_kernel<kMaxThreads, 1>, dim3(a.num_tokens), dim3(warps * 32),
+                    0, stream, a);
 }
 
 }  // namespace pkvqk
