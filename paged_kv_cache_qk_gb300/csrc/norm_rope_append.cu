@@ -20,10 +20,12 @@
 //  * the RMS scale r = rsqrt(mean(x^2) + eps) multiplies the rotated value
 //    last (a common factor, it contributes only relative error).
 // Each head vector (D = 128 bf16 = 256 B) is handled by a half-warp: lane l
-// holds elements [8l, 8l+8) as one 16-byte load; the sum of squares is a
-// 4-step xor-shuffle reduction inside the half-warp, and the rotate-half
-// partner of lane l is lane l ^ 8.  A half-warp takes up to kHoist vectors of
-// its token, and issues all their loads before the angle work.  Few tokens
+// holds elements [4l, 4l+4) and their rotate-half partners [64+4l, 64+4l+4)
+// (two 8-byte loads), so a rotation needs no shuffle, and keeps the sin/cos
+// of its four frequencies in registers for every vector of the token; the
+// sum of squares is a 4-step xor-shuffle reduction inside the half-warp.  A
+// half-warp takes up to kHoist vectors of its token, and issues all their
+// loads before the angle work.  Few tokens
 // (decode): one half-warp per vector, the shortest path per token.  Many
 // tokens (prefill chunks): three or more warps per token and up to four
 // vectors per half-warp, so several tokens per SM overlap their latencies.
@@ -45,88 +47,114 @@ constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
 constexpr int kManyThreads = 96;
 constexpr int kManyMinBlocks = 8;
 
+// A lane's part of one head vector: elements [4l, 4l + 4) and their
+// rotate-half partners [64 + 4l, 64 + 4l + 4), as raw bf16 (x, and v for kv
+// heads).
 struct Loaded {
-  uint4 x, v;
+  uint2 x0, x1, v0, v1;
 };
+
+// sin/cos of this lane's four frequencies 4l .. 4l+3, float-float pairs.
+struct Trig {
+  float4 ch, cl, sh, sl;
+};
+
+__device__ __forceinline__ void unpack4(const uint2& u, float* f) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+}
 
 // Loads x (and for k heads the v row) of head vector h of token t.
 __device__ __forceinline__ Loaded load_vector(const NormRopeAppendArgs& a, int t, int h, int l) {
   Loaded r;
-  r.x = r.v = make_uint4(0, 0, 0, 0);
+  r.x0 = r.x1 = r.v0 = r.v1 = make_uint2(0, 0);
   if (h < a.num_q_heads) {
-    r.x = *reinterpret_cast<const uint4*>(a.q + t * a.q_stride_t +
-                                          static_cast<int64_t>(h) * a.q_stride_h + l * 8);
+    const __nv_bfloat16* src = a.q + t * a.q_stride_t + static_cast<int64_t>(h) * a.q_stride_h;
+    r.x0 = *reinterpret_cast<const uint2*>(src + 4 * l);
+    r.x1 = *reinterpret_cast<const uint2*>(src + 64 + 4 * l);
   } else if (h < a.num_q_heads + a.num_kv_heads) {
     const int hk = h - a.num_q_heads;
-    r.x = __ldg(reinterpret_cast<const uint4*>(a.k + t * a.k_stride_t +
-                                               static_cast<int64_t>(hk) * a.k_stride_h + l * 8));
-    r.v = __ldg(reinterpret_cast<const uint4*>(a.v + t * a.v_stride_t +
-                                               static_cast<int64_t>(hk) * a.v_stride_h + l * 8));
+    const __nv_bfloat16* ks = a.k + t * a.k_stride_t + static_cast<int64_t>(hk) * a.k_stride_h;
+    const __nv_bfloat16* vs = a.v + t * a.v_stride_t + static_cast<int64_t>(hk) * a.v_stride_h;
+    r.x0 = __ldg(reinterpret_cast<const uint2*>(ks + 4 * l));
+    r.x1 = __ldg(reinterpret_cast<const uint2*>(ks + 64 + 4 * l));
+    r.v0 = __ldg(reinterpret_cast<const uint2*>(vs + 4 * l));
+    r.v1 = __ldg(reinterpret_cast<const uint2*>(vs + 64 + 4 * l));
   }
   return r;
 }
 
+// r * (a c - b s) for c = ch + cl, s = sh + sl: the products a*ch and b*sh
+// error-free (p + e), the low parts and the error terms added last.
+__device__ __forceinline__ float rotate(float a, float b, float ch, float cl, float sh, float sl,
+                                        float r) {
+  const float p1 = a * ch, e1 = fmaf(a, ch, -p1);   // a*c_hi = p1 + e1 exactly
+  const float p2 = -b * sh, e2 = fmaf(-b, sh, -p2); // -b*s_hi = p2 + e2 exactly
+  const float tail = fmaf(a, cl, -b * sl) + (e1 + e2);
+  return r * ((p1 + p2) + tail);
+}
+
 // Norm + rotation + stores of one head vector; both half-warps of the warp
-// call it together (every shuffle is warp-wide).
+// call it together (the sum-of-squares shuffles are warp-wide).
 __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t, int h, int l,
-                                              const Loaded& in, const uint4& gq, const uint4& gk,
-                                              int64_t cache_row,
-                                              bool write_cache, const float* s_cos_hi,
-                                              const float* s_cos_lo, const float* s_sin_hi,
-                                              const float* s_sin_lo) {
+                                              const Loaded& in, const uint2 (&gq)[2],
+                                              const uint2 (&gk)[2], int64_t cache_row,
+                                              bool write_cache, const Trig& tr) {
   const int num_vec = a.num_q_heads + a.num_kv_heads;
-  float x[8], g[8];
-  unpack8(in.x, x);
-  unpack8(h < a.num_q_heads ? gq : gk, g);
+  float x0[4], x1[4], g0[4], g1[4];
+  unpack4(in.x0, x0);
+  unpack4(in.x1, x1);
+  const bool is_q = h < a.num_q_heads;
+  unpack4(is_q ? gq[0] : gk[0], g0);
+  unpack4(is_q ? gq[1] : gk[1], g1);
   // x*gamma is exact in fp32; x^2 is exact, the sum rounds
-  float ss = 0.f, ag[8];
+  float ss = 0.f, a0[4], a1[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    ss = fmaf(x[j], x[j], ss);
-    ag[j] = x[j] * g[j];
+  for (int j = 0; j < 4; ++j) {
+    ss = fmaf(x0[j], x0[j], ss);
+    ss = fmaf(x1[j], x1[j], ss);
+    a0[j] = x0[j] * g0[j];
+    a1[j] = x1[j] * g1[j];
   }
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float r = rsqrtf(fmaf(ss, 1.0f / kHeadDim, a.eps));
 
-  // rotate-half: lanes 0..7 hold a[i], lanes 8..15 hold a[i + D/2];
-  // out_i = a_i c - a_{i+D/2} s,  out_{i+D/2} = a_{i+D/2} c + a_i s
-  const int fbase = (l & 7) * 8;
-  const float sgn = (l < 8) ? -1.f : 1.f;
-  float out[8];
+  // rotate-half, pair (i, i + D/2) in this lane:
+  //   out_i = a_i c - a_{i+D/2} s,   out_{i+D/2} = a_{i+D/2} c + a_i s
+  const float ch[4] = {tr.ch.x, tr.ch.y, tr.ch.z, tr.ch.w};
+  const float cl[4] = {tr.cl.x, tr.cl.y, tr.cl.z, tr.cl.w};
+  const float sh[4] = {tr.sh.x, tr.sh.y, tr.sh.z, tr.sh.w};
+  const float sl[4] = {tr.sl.x, tr.sl.y, tr.sl.z, tr.sl.w};
+  float o0[4], o1[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float b = sgn * __shfl_xor_sync(0xffffffffu, ag[j], 8);
-    const float ch = s_cos_hi[fbase + j], cl = s_cos_lo[fbase + j];
-    const float sh = s_sin_hi[fbase + j], sl = s_sin_lo[fbase + j];
-    const float p1 = ag[j] * ch, e1 = fmaf(ag[j], ch, -p1);   // a*c_hi = p1 + e1 exactly
-    const float p2 = b * sh, e2 = fmaf(b, sh, -p2);           // b*s_hi = p2 + e2 exactly
-    const float tail = fmaf(ag[j], cl, b * sl) + (e1 + e2);
-    out[j] = r * ((p1 + p2) + tail);
+  for (int j = 0; j < 4; ++j) {
+    o0[j] = rotate(a0[j], a1[j], ch[j], cl[j], sh[j], sl[j], r);
+    o1[j] = rotate(a1[j], -a0[j], ch[j], cl[j], sh[j], sl[j], r);
   }
-  uint4 ov;
-  ov.x = pack_bf16x2(out[0], out[1]);
-  ov.y = pack_bf16x2(out[2], out[3]);
-  ov.z = pack_bf16x2(out[4], out[5]);
-  ov.w = pack_bf16x2(out[6], out[7]);
+  const uint2 w0 = make_uint2(pack_bf16x2(o0[0], o0[1]), pack_bf16x2(o0[2], o0[3]));
+  const uint2 w1 = make_uint2(pack_bf16x2(o1[0], o1[1]), pack_bf16x2(o1[2], o1[3]));
 
   if (h >= num_vec) return;
-  if (h < a.num_q_heads) {
-    *reinterpret_cast<uint4*>(a.q + t * a.q_stride_t + static_cast<int64_t>(h) * a.q_stride_h +
-                              l * 8) = ov;
+  if (is_q) {
+    __nv_bfloat16* dst = a.q + t * a.q_stride_t + static_cast<int64_t>(h) * a.q_stride_h;
+    *reinterpret_cast<uint2*>(dst + 4 * l) = w0;
+    *reinterpret_cast<uint2*>(dst + 64 + 4 * l) = w1;
   } else if (write_cache) {
     const int hk = h - a.num_q_heads;
-    const int64_t dst = cache_row + static_cast<int64_t>(hk) * a.head_stride + l * 8;
-    *reinterpret_cast<uint4*>(a.k_cache + dst) = ov;
-    *reinterpret_cast<uint4*>(a.v_cache + dst) = in.v;
+    const int64_t row = cache_row + static_cast<int64_t>(hk) * a.head_stride;
+    *reinterpret_cast<uint2*>(a.k_cache + row + 4 * l) = w0;
+    *reinterpret_cast<uint2*>(a.k_cache + row + 64 + 4 * l) = w1;
+    *reinterpret_cast<uint2*>(a.v_cache + row + 4 * l) = in.v0;
+    *reinterpret_cast<uint2*>(a.v_cache + row + 64 + 4 * l) = in.v1;
   }
 }
 
 template <int kThreadsBound, int kMinBlocks>
 __global__ void __launch_bounds__(kThreadsBound, kMinBlocks)
 norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
-  __shared__ float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
-  __shared__ float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
+  __shared__ __align__(16) float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
+  __shared__ __align__(16) float s_sin_hi[kHeadDim / 2], s_sin_lo[kHeadDim / 2];
   __shared__ float s_tab[kSinCosKnots][4];
 
   const int t = blockIdx.x;
@@ -147,9 +175,11 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   Loaded in[kHoist];
 #pragma unroll
   for (int p = 0; p < kHoist; ++p) in[p] = load_vector(a, t, h0 + p * vec_per_pass, l);
-  // the gains are the same for every token and head: one load per lane
-  const uint4 gq = __ldg(reinterpret_cast<const uint4*>(a.gamma_q + l * 8));
-  const uint4 gk = __ldg(reinterpret_cast<const uint4*>(a.gamma_k + l * 8));
+  // the gains are the same for every token and head: loaded once per lane
+  const uint2 gq[2] = {__ldg(reinterpret_cast<const uint2*>(a.gamma_q + 4 * l)),
+                       __ldg(reinterpret_cast<const uint2*>(a.gamma_q + 64 + 4 * l))};
+  const uint2 gk[2] = {__ldg(reinterpret_cast<const uint2*>(a.gamma_k + 4 * l)),
+                       __ldg(reinterpret_cast<const uint2*>(a.gamma_k + 64 + 4 * l))};
   // the sin/cos knots to shared memory while those loads are in flight: the
   // lookups below take a different knot in every lane, and indexing the
   // parameter copy that way costs one constant-cache access per distinct
@@ -178,6 +208,12 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   const int64_t off = write_cache ? slot % a.block_size : 0;
   const int64_t cache_row = blk * a.block_stride + off * a.slot_stride;
   __syncthreads();
+  // this lane's four frequencies, for every head vector it finishes
+  Trig tr;
+  tr.ch = *reinterpret_cast<const float4*>(s_cos_hi + 4 * l);
+  tr.cl = *reinterpret_cast<const float4*>(s_cos_lo + 4 * l);
+  tr.sh = *reinterpret_cast<const float4*>(s_sin_hi + 4 * l);
+  tr.sl = *reinterpret_cast<const float4*>(s_sin_lo + 4 * l);
 
   // warp-uniform: both half-warps of a warp share `base`
   const int num_vec = a.num_q_heads + a.num_kv_heads;
@@ -185,15 +221,13 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   for (int p = 0; p < kHoist; ++p) {
     const int base = warp * 2 + p * vec_per_pass;
     if (base < num_vec)
-      finish_vector(a, t, base + (lane >> 4), l, in[p], gq, gk, cache_row, write_cache, s_cos_hi,
-                    s_cos_lo, s_sin_hi, s_sin_lo);
+      finish_vector(a, t, base + (lane >> 4), l, in[p], gq, gk, cache_row, write_cache, tr);
   }
   // more head vectors than kHoist passes cover (Hq + Hkv > 2 * kHoist * warps)
   for (int base = warp * 2 + kHoist * vec_per_pass; base < num_vec; base += vec_per_pass) {
     const int h = base + (lane >> 4);
     const Loaded in = load_vector(a, t, h, l);
-    finish_vector(a, t, h, l, in, gq, gk, cache_row, write_cache, s_cos_hi, s_cos_lo, s_sin_hi,
-                  s_sin_lo);
+    finish_vector(a, t, h, l, in, gq, gk, cache_row, write_cache, tr);
   }
 }
 
