@@ -370,12 +370,9 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
     return fail(PKVQK_ERR_INVALID_ARG, "q strides must be multiples of 8 elements");
   if (!std::isfinite(c.scale)) return fail(PKVQK_ERR_INVALID_ARG, "scale is not finite");
   const int S = c.num_splits;
-  // CTA pairs (M = 256 MMAs over two SMs) once a kv head has more rows than
-  // one CTA holds
-  const bool pair = rows > pkvqk::kPrefillRowsPerCta;
-  const int unit_rows = pair ? 2 * pkvqk::kPrefillRowsPerCta : pkvqk::kPrefillRowsPerCta;
-  const int m_tiles = static_cast<int>((rows + unit_rows - 1) / unit_rows);
-  const int64_t grid_x = static_cast<int64_t>(m_tiles) * L.num_kv_heads * S * (pair ? 2 : 1);
+  const int m_tiles = static_cast<int>((rows + pkvqk::kPrefillRowsPerCta - 1) /
+                                       pkvqk::kPrefillRowsPerCta);
+  const int64_t grid_x = static_cast<int64_t>(m_tiles) * L.num_kv_heads * S;
   if (grid_x > INT32_MAX) return fail(PKVQK_ERR_UNSUPPORTED, "too many CTAs (%lld)",
                                       static_cast<long long>(grid_x));
   const int64_t nrows = total_q * c.num_q_heads;
@@ -407,8 +404,9 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
   }
   if (c.status_flags != nullptr) PKVQK_TRY(check_device_ptr(c.status_flags, "status_flags"));
 
-  // a power of two dividing the page size: no box crosses a page
-  const int box_slots = pkvqk::prefill_box_slots(L.block_size, pair);
+  // largest power of two dividing the page size, at most 128 (the kernel's
+  // key tile): no box crosses a page
+  const int box_slots = std::min(L.block_size & -L.block_size, 128);
   CUtensorMap kmap, vmap;
   PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, 1, box_slots, 1));
   PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, 1, box_slots, 1));
@@ -434,7 +432,6 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
   a.num_splits = S;
   a.chunk_pages = std::max(1, (hint_pages + S - 1) / S);
   a.m_tiles = m_tiles;
-  a.box_slots = box_slots;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(128.0f);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = static_cast<__nv_bfloat16*>(c.out);
@@ -443,7 +440,7 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
   a.ws_lse = S > 1 ? a.ws_o + nrows * S * 128 : nullptr;
   a.status_flags = c.status_flags;
 
-  cudaError_t e = pkvqk::launch_paged_prefill(kmap, vmap, a, pair, c.stream);
+  cudaError_t e = pkvqk::launch_paged_prefill(kmap, vmap, a, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
   if (S > 1 && !c.partials_only) {
     e = pkvqk::launch_lse_combine(a.ws_o, a.ws_lse, static_cast<int>(nrows), S, a.out, c.lse_out,

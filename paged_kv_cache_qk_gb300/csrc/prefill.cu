@@ -14,28 +14,12 @@
 // from cumulative row offsets; the grid covers the longest, and row tiles past
 // a shorter sequence's rows do nothing.
 //
-// Two forms of one kernel, chosen per call by the host:
-//
-// * Single CTA.  One CTA = two tiles A and B of 128 packed rows
-//   r = t * group + (h % group) of one (sequence, kv head) -- 256 consecutive
-//   rows -- restricted to one split of the key range.  Keys stream in tiles of
-//   128 through two-stage TMA rings (K and V separately).
-// * CTA pair (a cluster of two CTAs on two SMs).  The pair owns 512
-//   consecutive rows: tile A = rows 0-255 of them, tile B = rows 256-511; CTA
-//   rank c holds rows c*128 .. c*128+127 of each, and rank 0 issues MMAs of
-//   M = 256 (tcgen05 cta_group::2) that read A from both CTAs and write D into
-//   both CTAs' tensor memory.  B is split by N: for S = Q K^T rank c stages
-//   keys c*64 .. c*64+63 of the key tile, for O += P V it stages dims
-//   c*64 .. c*64+63 of all 128 keys, so each SM reads half of every B operand
-//   from its shared memory and the per-stage footprint halves (four-stage
-//   rings).  Rank 1's TMA completions reach rank 0 through a relay thread
-//   (rank 1's otherwise idle MMA lane) that arrives on rank-0 barriers; its
-//   softmax warps arrive on rank 0's P barrier the same way; rank 0's MMA
-//   commits arrive on both CTAs' barriers (multicast).
-//
-// In both forms both row tiles use every key tile, and the tensor core
-// alternates between them so that one tile's softmax runs while the other
-// tile's MMAs do (ping-pong).  Warp roles (per CTA):
+// One CTA = two tiles A and B of 128 packed rows r = t * group + (h % group)
+// of one (sequence, kv head) -- 256 consecutive rows -- restricted to one
+// split of the key range.  Keys stream in tiles of 128 through two-stage TMA
+// rings (K and V separately); both row tiles use every key tile, and the
+// tensor core alternates between them so that one tile's softmax runs while
+// the other tile's MMAs do (ping-pong).  Warp roles:
 //   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (tensor-memory
 //              lane r).  Reads its score row S = Q K^T from tensor memory,
 //              keeps the running max and sum, writes P (bf16 pairs) back into
@@ -45,11 +29,10 @@
 //   warp 8     TMA producer: one box per (page, 64-dim half) of K and of V;
 //   warp 9     allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
-//              (pair: rank 0 only; rank 1's lane 0 is the relay)
-//              S_x = Q_x K_i^T  (N 128 keys, K 128 dims; both operands in
-//                               shared memory),
-//              O_x += P_x V_i   (N 128 dims, K 128 keys; P from tensor
-//                               memory, V from shared memory).
+//              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
+//                               operands in shared memory),
+//              O_x += P_x V_i   (M 128 rows, N 128 dims, K 128 keys; P from
+//                               tensor memory, V from shared memory).
 // S_x(i+1) overwrites the columns that held P_x(i): the MMAs of one thread
 // run in issue order, and PV_x(i) is issued first.  The commit that signals
 // S_x(i+1) also covers PV_x(i), so softmax x may rescale O_x as soon as it
@@ -57,34 +40,33 @@
 //
 // Shared memory (1024-byte aligned, 128-byte swizzle everywhere, the layout
 // the MMA descriptors describe):
-//   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]                2 x 32 KiB
-//   single CTA: K stage, V stage [2 dim halves][128 keys][64]   2 x (32 + 32) KiB
-//   pair:       K stage [2 dim halves][64 keys][64],
-//               V stage [128 keys][64 bf16] (this CTA's dims)  4 x (16 + 16) KiB
+//   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]      2 x 32 KiB
+//   K stage s [2 dim halves][128 keys][64 bf16]      2 x 32 KiB
+//   V stage s  the same                              2 x 32 KiB
 // Tensor memory: S_A (then P_A) at columns 0-127, S_B (P_B) 128-255, O_A
 // 256-383, O_B 384-511.
 //
 // Every wait is bounded: on a timeout the CTA reports PKVQK_FLAG_WAIT_TIMEOUT,
 // lets its own copies and MMAs in flight finish (bounded), frees its tensor
-// memory and exits (a pair meets at a cluster barrier first, so neither CTA
-// leaves while the other's MMAs may still read its memory).
-#include "cluster.cuh"
+// memory and exits.
 #include "device_common.cuh"
 #include "prefill.h"
 #include "tc5.cuh"
-
-#include <algorithm>
 
 namespace pkvqk {
 
 namespace {
 
-constexpr int kM = 128;                        // rows per row tile (per CTA)
+constexpr int kM = 128;                        // rows per row tile
 constexpr int kN = 128;                        // keys per key tile
 static_assert(2 * kM == kPrefillRowsPerCta, "two row tiles per CTA");
 constexpr int kHalf = 128 * 128;               // [128 rows][64 bf16] sub-tile, bytes
 constexpr int kTile = 2 * kHalf;               // [128 rows][128 bf16], bytes
-constexpr int kMaxStages = 4;
+constexpr int kStages = 2;
+constexpr int kOffQ = 0;                       // Q_A, Q_B
+constexpr int kOffK = 2 * kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kDataBytes = kOffV + kStages * kTile;
 constexpr int kThreads = 10 * 32;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -94,30 +76,9 @@ constexpr uint32_t kColO = 256;                // + x * kN
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Stage geometry of the two forms.
-template <bool kPair>
-struct Form {
-  static constexpr int kStages = kPair ? 4 : 2;
-  static constexpr int kKeysK = kPair ? 64 : 128;          // keys of a K stage
-  static constexpr int kKHalfOff = kKeysK * 128;           // bytes between its dim halves
-  static constexpr int kKBytes = 2 * kKHalfOff;
-  static constexpr int kVHalves = kPair ? 1 : 2;           // dim halves of a V stage
-  static constexpr int kVBytes = kVHalves * kHalf;
-  static constexpr int kOffQ = 0;                          // Q_A, Q_B
-  static constexpr int kOffK = 2 * kTile;
-  static constexpr int kOffV = kOffK + kStages * kKBytes;
-  static constexpr int kDataBytes = kOffV + kStages * kVBytes;
-  static constexpr int kUnitRows = kPair ? 4 * kM : 2 * kM;   // rows of a CTA / pair
-  static constexpr int kTileStride = kUnitRows / 2;           // tile A row 0 -> tile B row 0
-  static constexpr int kMmaM = kPair ? 2 * kM : kM;
-  static_assert(kStages <= kMaxStages, "barrier arrays");
-};
-static_assert(Form<false>::kDataBytes == Form<true>::kDataBytes, "one shared-memory size");
-
 struct Bars {
-  uint64_t full_k[kMaxStages], full_v[kMaxStages];     // this CTA's TMA landed
-  uint64_t empty_k[kMaxStages], empty_v[kMaxStages];   // the MMAs reading a stage finished
-  uint64_t peer_k[kMaxStages], peer_v[kMaxStages];     // pair, rank 0: rank 1's copies landed
+  uint64_t full_k[kStages], full_v[kStages];     // TMA landed
+  uint64_t empty_k[kStages], empty_v[kStages];   // the MMAs reading a stage finished
   uint64_t s_full[2];                            // S_x written (and the PV before it done)
   uint64_t p_full[2];                            // P_x written (and O_x rescaled)
   uint64_t pv_done[2];                           // the last O_x += P_x V finished
@@ -125,25 +86,24 @@ struct Bars {
   uint32_t tmem_base;
   int32_t abort;
 };
-static_assert(sizeof(Bars) <= 512, "barrier block");
-constexpr int kSmemBytes = Form<false>::kDataBytes + 512 + 1024;   // + barriers + alignment slack
+static_assert(sizeof(Bars) <= 256, "barrier block");
+constexpr int kSmemBytes = kDataBytes + 256 + 1024;   // + barriers + alignment slack
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_addr(p);
   return p + (((s + 1023u) & ~1023u) - s);
 }
 
-// A [rows][128 bf16] operand stored as two 64-wide swizzled halves `half_off`
-// bytes apart, read K-major in 16-element steps: step kk is 32 bytes into the
-// rows of half kk/4; 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_k_major(uint32_t tile, int kk, int half_off) {
-  return tc5::smem_desc_sw128(tile + (kk >> 2) * half_off + (kk & 3) * 32, 16, 1024);
+// A [128 rows][128 bf16] operand stored as two 64-wide swizzled halves, read
+// K-major in 16-element steps: step kk is 32 bytes into the rows of half kk/4;
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_k_major(uint32_t tile, int kk) {
+  return tc5::smem_desc_sw128(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
 }
 
-// V stage as the MN-major B operand of O += P V (N = dims, K = keys): 64 dims
-// per swizzled row, the two dim halves kHalf apart (leading offset; a pair's
-// stage holds one half, so it is not used there), 8-key groups 1024 bytes
-// apart (stride offset); 16-key step ks starts 2048 bytes on.
+// V tile as the MN-major B operand of O += P V (N = dims, K = keys): 64 dims
+// per swizzled row, the two dim halves kHalf apart (leading offset), 8-key
+// groups 1024 bytes apart (stride offset); 16-key step ks starts 2048 bytes on.
 __device__ __forceinline__ uint64_t desc_v(uint32_t vtile, int ks) {
   return tc5::smem_desc_sw128(vtile + ks * 2048, kHalf, 1024);
 }
@@ -160,27 +120,16 @@ __device__ __forceinline__ void tma_load_5d_keep(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Waits on barriers that another CTA of the pair may arrive on take cluster
-// scope; a single CTA's are local.
-template <bool kPair>
-__device__ __forceinline__ bool wait_any(uint64_t* bar, uint32_t parity) {
-  return kPair ? mbar_wait_cluster(bar, parity) : mbar_wait(bar, parity);
-}
-
-template <bool kPair>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-  const bool ok = wait_any<kPair>(bar, parity);
+  const bool ok = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, ok);
 }
 
 struct Work {
   int b, g, j, mt;
-  int rank;      // cluster rank (0 for a single CTA)
-  int unit0;     // first row of the CTA's (pair's) 256 (512) rows
-  int row0;      // first row of this CTA's part of tile A
   int L;         // keys of the sequence (clamped to the table)
   int k0, k1;    // the split's key range
-  int key_end;   // keys at or past key_end are visible to no row of the CTA (pair)
+  int key_end;   // keys at or past key_end are visible to no row of the CTA
   int ntiles;
   int q_len;     // this sequence's new tokens
   long long q0;  // row of q/out holding its token 0
@@ -188,13 +137,9 @@ struct Work {
   bool has_b;    // row tile B holds rows
 };
 
-// Both CTAs of a pair compute the same unit, key range, tile count and has_b.
-template <bool kPair>
 __device__ Work decode_work(const PrefillArgs& a) {
-  using F = Form<kPair>;
   Work w;
-  w.rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
-  int x = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  int x = blockIdx.x;
   w.mt = x % a.m_tiles;
   x /= a.m_tiles;
   w.g = x % a.num_kv_heads;
@@ -215,60 +160,46 @@ __device__ Work decode_work(const PrefillArgs& a) {
     w.q_len = a.q_len;
   }
   w.rows = w.q_len * a.group;
-  w.unit0 = w.mt * F::kUnitRows;
-  w.row0 = w.unit0 + w.rank * kM;
-  w.has_b = w.unit0 + F::kTileStride < w.rows;
-  const int last_row = min(w.unit0 + F::kUnitRows - 1, w.rows - 1);
+  const int row0 = w.mt * 2 * kM;
+  w.has_b = row0 + kM < w.rows;
+  const int last_row = min(row0 + 2 * kM - 1, w.rows - 1);
   const int t_last = last_row / a.group;
   w.key_end = max(w.k0, min(w.k1, w.L - w.q_len + t_last + 1));
-  w.ntiles = w.unit0 < w.rows ? (w.key_end - w.k0 + kN - 1) / kN : 0;
+  w.ntiles = row0 < w.rows ? (w.key_end - w.k0 + kN - 1) / kN : 0;
   return w;
 }
 
 // ------------------------------------------------------------- producer
 
-template <bool kPair>
 __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, uint8_t* smem, Bars* bars, int* issued_out) {
-  using F = Form<kPair>;
   const int lane = threadIdx.x & 31;
   const int bs = a.block_size;
-  // slots per box (the host's power of two dividing the page size, at most
-  // the keys of a K stage); boxes start at multiples of it, so none crosses a
-  // page
-  const int tb = a.box_slots;
-  const int nbk = F::kKeysK / tb;               // K boxes per stage
-  const int nbv = kN / tb;                      // V boxes per stage
+  // slots per box: the largest power of two dividing the page size, at most
+  // a key tile; a tile's boxes start at multiples of it, so none crosses a page
+  const int tb = min(bs & -bs, kN);
+  const int ppt = kN / tb;                      // boxes per key tile
   const int32_t* bt = a.block_tables + static_cast<long long>(w.b) * a.max_blocks_per_seq;
   const int oob = static_cast<int>(a.num_blocks);   // past the extent: TMA fills zeros
-  // the block holding `key` and the key's slot in it (oob at or past key_end)
-  auto lookup = [&](int key, int& blk, int& slot0) {
-    const int page = key / bs;
-    slot0 = key - page * bs;
-    blk = oob;
-    if (key < w.key_end) {
-      const int id = __ldg(bt + page);
-      if (id >= 0 && static_cast<long long>(id) < a.num_blocks) blk = id;
-      else report(a.status_flags, kFlagBadBlock);
-    }
-  };
   int issued = 0;
   for (int i = 0; i < w.ntiles; ++i) {
-    const int s = i % F::kStages;
-    const uint32_t rel = ((i / F::kStages) - 1) & 1;    // release of tile i - kStages
-    uint8_t* kt = smem + F::kOffK + s * F::kKBytes;
-    uint8_t* vt = smem + F::kOffV + s * F::kVBytes;
-    const int kb = w.k0 + i * kN;
-    int blk_k = oob, slot_k = 0, blk_v = oob, slot_v = 0;
-    if (lane < nbk) lookup(kb + w.rank * F::kKeysK + lane * tb, blk_k, slot_k);
-    if constexpr (kPair) {
-      if (lane < nbv) lookup(kb + lane * tb, blk_v, slot_v);
-    } else {
-      blk_v = blk_k;                            // the same 128 keys
-      slot_v = slot_k;
+    const int s = i & 1;
+    const uint32_t rel = ((i >> 1) - 1) & 1;         // release of tile i - 2
+    uint8_t* kt = smem + kOffK + s * kTile;
+    uint8_t* vt = smem + kOffV + s * kTile;
+    int blk = oob, slot0 = 0;
+    if (lane < ppt) {
+      const int key = w.k0 + i * kN + lane * tb;   // first key of box `lane`
+      const int page = key / bs;
+      slot0 = key - page * bs;
+      if (key < w.key_end) {
+        const int id = __ldg(bt + page);
+        if (id >= 0 && static_cast<long long>(id) < a.num_blocks) blk = id;
+        else report(a.status_flags, kFlagBadBlock);
+      }
     }
     bool ok = true;
-    if (lane == 0 && i >= F::kStages) ok = wait_any<kPair>(&bars->empty_k[s], rel);
+    if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_k[s], rel);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
       if (lane == 0) {
@@ -277,14 +208,14 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
       }
       break;
     }
-    if (lane == 0) mbar_arrive_expect_tx(&bars->full_k[s], F::kKBytes);
+    if (lane == 0) mbar_arrive_expect_tx(&bars->full_k[s], kTile);
     __syncwarp();
-    if (lane < nbk) {
-      tma_load_5d_keep(kt + lane * tb * 128, kmap, &bars->full_k[s], 0, slot_k, 0, w.g, blk_k);
-      tma_load_5d_keep(kt + F::kKHalfOff + lane * tb * 128, kmap, &bars->full_k[s], 0, slot_k, 1,
-                       w.g, blk_k);
+    if (lane < ppt) {
+      tma_load_5d_keep(kt + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 0, w.g, blk);
+      tma_load_5d_keep(kt + kHalf + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 1, w.g,
+                       blk);
     }
-    if (lane == 0 && i >= F::kStages) ok = wait_any<kPair>(&bars->empty_v[s], rel);
+    if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_v[s], rel);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
       if (lane == 0) {
@@ -294,17 +225,12 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
       issued = -(i + 1);                            // K of tile i is in flight, V is not
       break;
     }
-    if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[s], F::kVBytes);
+    if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[s], kTile);
     __syncwarp();
-    if (lane < nbv) {
-      if constexpr (kPair) {
-        tma_load_5d_keep(vt + lane * tb * 128, vmap, &bars->full_v[s], 0, slot_v, w.rank, w.g,
-                         blk_v);
-      } else {
-        tma_load_5d_keep(vt + lane * tb * 128, vmap, &bars->full_v[s], 0, slot_v, 0, w.g, blk_v);
-        tma_load_5d_keep(vt + kHalf + lane * tb * 128, vmap, &bars->full_v[s], 0, slot_v, 1, w.g,
-                         blk_v);
-      }
+    if (lane < ppt) {
+      tma_load_5d_keep(vt + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 0, w.g, blk);
+      tma_load_5d_keep(vt + kHalf + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 1, w.g,
+                       blk);
     }
     issued = i + 1;
   }
@@ -312,99 +238,53 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
 }
 
 // After a timeout: wait (bounded) for the last copies issued into each stage.
-template <bool kPair>
 __device__ void drain_copies(Bars* bars, int issued) {
-  using F = Form<kPair>;
   const bool v_missing = issued < 0;
   const int n = v_missing ? -issued : issued;
-  for (int i = n - F::kStages < 0 ? 0 : n - F::kStages; i < n; ++i) {
-    const int s = i % F::kStages;
-    const uint32_t par = (i / F::kStages) & 1;
-    mbar_wait(&bars->full_k[s], par);
-    if (!(v_missing && i == n - 1)) mbar_wait(&bars->full_v[s], par);
-  }
-}
-
-// Pair, rank 1: pass each stage's completion on to rank 0, whose MMAs read
-// this CTA's half of it.  Runs on the lane that issues the MMAs on rank 0.
-__device__ void relay_copies(const PrefillArgs& a, const Work& w, Bars* bars) {
-  using F = Form<true>;
-  for (int i = 0; i < w.ntiles; ++i) {
-    const int s = i % F::kStages;
-    const uint32_t par = (i / F::kStages) & 1;
-    if (!mbar_wait(&bars->full_k[s], par)) {
-      bars->abort = 1;
-      report(a.status_flags, kFlagTimeout);
-      return;
-    }
-    mbar_arrive_remote(cluster_addr(&bars->peer_k[s], 0));
-    if (!mbar_wait(&bars->full_v[s], par)) {
-      bars->abort = 1;
-      report(a.status_flags, kFlagTimeout);
-      return;
-    }
-    mbar_arrive_remote(cluster_addr(&bars->peer_v[s], 0));
+  for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i) {
+    const int s = i & 1;
+    mbar_wait(&bars->full_k[s], (i >> 1) & 1);
+    if (!(v_missing && i == n - 1)) mbar_wait(&bars->full_v[s], (i >> 1) & 1);
   }
 }
 
 // ------------------------------------------------------------ MMA issue
 
-template <bool kPair>
-__device__ __forceinline__ void commit_to(uint64_t* bar) {
-  if constexpr (kPair) tc5::commit_pair(bar, 0x3);   // the barrier in both CTAs
-  else tc5::commit(bar);
-}
-
-// Single CTA, or rank 0 of a pair.
-template <bool kPair>
 __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
                            uint32_t tmem) {
-  using F = Form<kPair>;
   const int last = w.has_b ? 1 : 0;            // the row tile that reads a stage last
   const int n = w.ntiles;
-  constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(F::kMmaM, kN, false);
-  constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(F::kMmaM, kHeadDim, true);
-  // this CTA's copies of stage s (and, in a pair, the other CTA's) landed
-  auto wait_stage = [&](uint64_t* full, uint64_t* peer, int i) -> bool {
-    const int s = i % F::kStages;
-    const uint32_t par = (i / F::kStages) & 1;
-    if (!mbar_wait(&full[s], par)) return false;
-    return !kPair || mbar_wait_cluster(&peer[s], par);
-  };
+  constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(kM, kN, false);
+  constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kM, kHeadDim, true);
   // S_x(i) = Q_x K_i^T
   auto mma_s = [&](int x, int i) -> bool {
-    const int s = i % F::kStages;
-    if (x == 0 && !wait_stage(bars->full_k, bars->peer_k, i)) return false;
+    const int s = i & 1;
+    if (x == 0 && !mbar_wait(&bars->full_k[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
-    const uint32_t q = smem_addr(smem + F::kOffQ + x * kTile);
-    const uint32_t kt = smem_addr(smem + F::kOffK + s * F::kKBytes);
+    const uint32_t q = smem_addr(smem + kOffQ + x * kTile);
+    const uint32_t kt = smem_addr(smem + kOffK + s * kTile);
 #pragma unroll
-    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-      const uint64_t da = desc_k_major(q, kk, kHalf), db = desc_k_major(kt, kk, F::kKHalfOff);
-      if constexpr (kPair) tc5::mma_f16_pair(tmem + kColS + x * kN, da, db, idesc_s, kk > 0 ? 1u : 0u);
-      else tc5::mma_f16(tmem + kColS + x * kN, da, db, idesc_s, kk > 0 ? 1u : 0u);
-    }
-    commit_to<kPair>(&bars->s_full[x]);
-    if (x == last) commit_to<kPair>(&bars->empty_k[s]);
+    for (int kk = 0; kk < kHeadDim / 16; ++kk)
+      tc5::mma_f16(tmem + kColS + x * kN, desc_k_major(q, kk), desc_k_major(kt, kk), idesc_s,
+                   kk > 0 ? 1u : 0u);
+    tc5::commit(&bars->s_full[x]);
+    if (x == last) tc5::commit(&bars->empty_k[s]);
     return true;
   };
   // O_x += P_x V_i
   auto mma_pv = [&](int x, int i) -> bool {
-    const int s = i % F::kStages;
-    if (!wait_any<kPair>(&bars->p_full[x], i & 1)) return false;
-    if (x == 0 && !wait_stage(bars->full_v, bars->peer_v, i)) return false;
+    const int s = i & 1;
+    if (!mbar_wait(&bars->p_full[x], i & 1)) return false;
+    if (x == 0 && !mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
-    const uint32_t vt = smem_addr(smem + F::kOffV + s * F::kVBytes);
+    const uint32_t vt = smem_addr(smem + kOffV + s * kTile);
     // P_x: 16 keys per step = 8 columns of bf16 pairs
 #pragma unroll
-    for (int ks = 0; ks < kN / 16; ++ks) {
-      const uint32_t d = tmem + kColO + x * kN, pa = tmem + kColS + x * kN + ks * 8;
-      const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-      if constexpr (kPair) tc5::mma_f16_ts_pair(d, pa, desc_v(vt, ks), idesc_pv, acc);
-      else tc5::mma_f16_ts(d, pa, desc_v(vt, ks), idesc_pv, acc);
-    }
-    if (i == n - 1) commit_to<kPair>(&bars->pv_done[x]);
-    if (x == last) commit_to<kPair>(&bars->empty_v[s]);
+    for (int ks = 0; ks < kN / 16; ++ks)
+      tc5::mma_f16_ts(tmem + kColO + x * kN, tmem + kColS + x * kN + ks * 8, desc_v(vt, ks),
+                      idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+    if (i == n - 1) tc5::commit(&bars->pv_done[x]);
+    if (x == last) tc5::commit(&bars->empty_v[s]);
     return true;
   };
   bool ok = true;
@@ -421,9 +301,8 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
   if (!ok) {
     bars->abort = 1;
     report(a.status_flags, kFlagTimeout);
-    if constexpr (kPair) tc5::commit_pair(&bars->drain, 0x1);   // everything issued so far ...
-    else tc5::commit(&bars->drain);
-    mbar_wait(&bars->drain, 0);                       // ... has finished
+    tc5::commit(&bars->drain);                 // everything issued so far ...
+    mbar_wait(&bars->drain, 0);                // ... has finished
   }
 }
 
@@ -509,11 +388,10 @@ __device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, f
 // The output rows of tile x: O / l (bf16, or the fp32 partial of the split)
 // and the log-sum-exp.  Kept out of line: the indices are recomputed here
 // instead of living in registers through the softmax loop.
-template <bool kPair>
 __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
                                         int x, float m_ref, float l) {
   const int r = threadIdx.x - x * kM;
-  const int rg = w.row0 + x * Form<kPair>::kTileStride + r;
+  const int rg = w.mt * 2 * kM + x * kM + r;
   const int t0 = rg / a.group;
   // rows outside the sequence, or (inconsistent offsets) outside q/out: no write;
   // every lane still takes part in the warp-wide tensor-memory loads below
@@ -574,13 +452,11 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
   }
 }
 
-template <bool kPair>
 __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
                              uint32_t tmem, int x) {
-  using F = Form<kPair>;
   const int r = threadIdx.x - x * kM;          // row of tile x = tensor-memory lane
   const int wq = r >> 5, lane = r & 31;
-  const int rg = w.row0 + x * F::kTileStride + r;
+  const int rg = w.mt * 2 * kM + x * kM + r;
   const bool valid = rg < w.rows;
   const int t = valid ? rg / a.group : 0;
   // keys [k0, lim) are visible to this row
@@ -589,15 +465,13 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   const uint32_t s_cols = lanes + kColS + x * kN;
   const uint32_t o_cols = lanes + kColO + x * kN;
   const float sl2 = a.scale_log2;
-  // where P_x's arrival goes: this CTA's barrier, or (pair, rank 1) rank 0's
-  const uint32_t p_remote = (kPair && w.rank != 0) ? cluster_addr(&bars->p_full[x], 0) : 0u;
 
   float m_ref = -INFINITY;                     // reference max (log2 units) of P
   float l = 0.f;                               // sum of P
   bool ok = true;
   for (int i = 0; i < w.ntiles; ++i) {
     // S_x(i) landed, and with it PV_x(i - 1): O_x is complete up to tile i - 1
-    if (!warp_wait<kPair>(&bars->s_full[x], i & 1)) {
+    if (!warp_wait(&bars->s_full[x], i & 1)) {
       ok = false;
       break;
     }
@@ -628,34 +502,31 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     l = l * alpha + psum;
     // Tail tile: cache slots past the last visible key may hold anything
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
-    // their V rows are zeroed (by tile A, in each CTA's own V stage, before
-    // either PV reads them).
+    // their V rows are zeroed (by tile A, before either PV reads them).
     if (x == 0 && kb + kN > w.key_end) {
-      const int s = i % F::kStages;
-      if (!warp_wait<false>(&bars->full_v[s], (i / F::kStages) & 1)) {
+      const int s = i & 1;
+      if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
         ok = false;
         break;
       }
       if (kb + r >= w.key_end) {
-        uint8_t* vrow = smem + F::kOffV + s * F::kVBytes + r * 128;
+        uint8_t* vrow = smem + kOffV + s * kTile + r * 128;
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int h = 0; h < F::kVHalves; ++h)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + h * kHalf + c * 16) = z;
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = z;
+          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
+        }
       }
       tc5::fence_smem_for_async();
     }
     tc5::wait_st();
     tc5::fence_before_sync();
     __syncwarp();
-    if (lane == 0) {
-      if (kPair && w.rank != 0) mbar_arrive_remote(p_remote);
-      else mbar_arrive(&bars->p_full[x]);
-    }
+    if (lane == 0) mbar_arrive(&bars->p_full[x]);
   }
   if (ok && w.ntiles > 0) {
-    ok = warp_wait<kPair>(&bars->pv_done[x], 0);
+    ok = warp_wait(&bars->pv_done[x], 0);
     tc5::fence_after_sync();
   }
   if (!ok) {
@@ -663,47 +534,42 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     report(a.status_flags, kFlagTimeout);
     return;
   }
-  write_rows<kPair>(a, w, tmem, x, m_ref, l);
+  write_rows(a, w, tmem, x, m_ref, l);
 }
 
 // ------------------------------------------------------------------ kernel
 
 // 10 warps: two of the SM's four sub-partitions hold three of them, so a
 // thread gets at most 168 registers (16,384 per sub-partition).
-template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
-  using F = Form<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  Bars* bars = reinterpret_cast<Bars*>(smem + F::kDataBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kDataBytes);
   __shared__ int issued;
   const int warp = threadIdx.x >> 5;
 
   // launched as a programmatic dependent: q, the appended K/V, the tables and
   // the lengths may come from the previous kernel in the stream
   pdl_wait();
-  const Work w = decode_work<kPair>(a);
+  const Work w = decode_work(a);
   // row tiles past this sequence's rows (varlen grids cover the longest
-  // sequence): nothing to compute or write; leave before any set-up (both
-  // CTAs of a pair decide alike, so neither waits for the other)
-  if (w.unit0 >= w.rows) return;
+  // sequence): nothing to compute or write; leave before any set-up
+  if (w.mt * 2 * kM >= w.rows) return;
 
   if (threadIdx.x == kProducerWarp * 32) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    for (int s = 0; s < F::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full_k[s], 1);
       mbar_init(&bars->full_v[s], 1);
       mbar_init(&bars->empty_k[s], 1);
       mbar_init(&bars->empty_v[s], 1);
-      mbar_init(&bars->peer_k[s], 1);
-      mbar_init(&bars->peer_v[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->p_full[x], kPair ? 8 : 4);   // a pair: both CTAs' four warps
+      mbar_init(&bars->p_full[x], 4);
       mbar_init(&bars->pv_done[x], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -711,16 +577,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     issued = 0;
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
-    if constexpr (kPair) tc5::tmem_alloc_pair(&bars->tmem_base, kTmemCols);
-    else tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
-  }
+  if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
 
   if (warp < 8) {
     // Q tiles: thread i loads row i % 128 of tile i / 128 (row = (token, q head
     // of the group)), two swizzled 64-dim halves
     const int x = threadIdx.x / kM, r = threadIdx.x % kM;
-    const int rg = w.row0 + x * F::kTileStride + r;
+    const int rg = w.mt * 2 * kM + threadIdx.x;
     const int t0 = rg / a.group;
     const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
     const int t = valid ? t0 : 0;
@@ -728,7 +591,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint4* src = reinterpret_cast<const uint4*>(
         a.q + (valid ? w.q0 + t : 0) * a.q_stride_t +
         static_cast<long long>(w.g * a.group + hh) * a.q_stride_h);
-    uint8_t* qt = smem + F::kOffQ + x * kTile;
+    uint8_t* qt = smem + kOffQ + x * kTile;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -737,39 +600,29 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     tc5::fence_smem_for_async();
   }
   tc5::fence_before_sync();
-  // a pair: each CTA's barriers, Q and tensor memory are ready before the
-  // other CTA's relay, arrivals or MMAs touch them
-  if constexpr (kPair) cluster_sync();
-  else __syncthreads();
+  __syncthreads();
   tc5::fence_after_sync();
   pdl_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < 4) {
-    softmax_rows<kPair>(a, w, smem, bars, tmem, 0);
+    softmax_rows(a, w, smem, bars, tmem, 0);
   } else if (warp < 8) {
-    if (w.has_b) softmax_rows<kPair>(a, w, smem, bars, tmem, 1);
+    if (w.has_b) softmax_rows(a, w, smem, bars, tmem, 1);
   } else if (warp == kProducerWarp) {
     int n = 0;
-    produce<kPair>(a, w, &kmap, &vmap, smem, bars, &n);
+    produce(a, w, &kmap, &vmap, smem, bars, &n);
     if (threadIdx.x == kProducerWarp * 32) issued = n;
   } else {
-    if ((threadIdx.x & 31) == 0) {
-      if (!kPair || w.rank == 0) issue_mmas<kPair>(a, w, smem, bars, tmem);
-      else relay_copies(a, w, bars);
-    }
+    if ((threadIdx.x & 31) == 0) issue_mmas(a, w, smem, bars, tmem);
     __syncwarp();
   }
   tc5::fence_before_sync();
   __syncthreads();
-  if (bars->abort && threadIdx.x == kProducerWarp * 32) drain_copies<kPair>(bars, issued);
-  // a pair: neither CTA frees its tensor memory or leaves while MMAs of rank 0
-  // may still read or write it
-  if constexpr (kPair) cluster_sync();
+  if (bars->abort && threadIdx.x == kProducerWarp * 32) drain_copies(bars, issued);
   if (warp == kMmaWarp) {
     tc5::fence_after_sync();
-    if constexpr (kPair) tc5::tmem_dealloc_pair(tmem, kTmemCols);
-    else tc5::tmem_dealloc(tmem, kTmemCols);
+    tc5::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -777,38 +630,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
 
 int prefill_smem_bytes() { return kSmemBytes; }
 
-int prefill_box_slots(int block_size, bool pair) {
-  return std::min(block_size & -block_size, pair ? Form<true>::kKeysK : Form<false>::kKeysK);
-}
-
 cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const PrefillArgs& a, bool pair, cudaStream_t stream) {
-  const long long units = static_cast<long long>(a.m_tiles) * a.num_kv_heads * a.num_splits;
-  if (!pair) {
-    static std::atomic<uint64_t> smem_set{0};
-    const cudaError_t e = set_smem_limit_once(paged_prefill_kernel<false>, kSmemBytes, smem_set);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(paged_prefill_kernel<false>, dim3(static_cast<unsigned>(units), a.batch),
-                      dim3(kThreads), kSmemBytes, stream, kmap, vmap, a);
-  }
-  static std::atomic<uint64_t> smem_set_pair{0};
-  const cudaError_t e = set_smem_limit_once(paged_prefill_kernel<true>, kSmemBytes, smem_set_pair);
+                                 const PrefillArgs& a, cudaStream_t stream) {
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(paged_prefill_kernel, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * units), a.batch);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<true>, kmap, vmap, a);
+  const long long gx = static_cast<long long>(a.m_tiles) * a.num_kv_heads * a.num_splits;
+  return launch_pdl(paged_prefill_kernel, dim3(static_cast<unsigned>(gx), a.batch),
+                    dim3(kThreads), kSmemBytes, stream, kmap, vmap, a);
 }
 
 }  // namespace pkvqk

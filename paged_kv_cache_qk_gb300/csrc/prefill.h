@@ -28,9 +28,7 @@ struct PrefillArgs {
   int64_t num_blocks;
   int32_t num_splits;              // >= 1
   int32_t chunk_pages;             // pages per split
-  int32_t m_tiles;                 // row units per (sequence, kv head, split):
-                                   // ceil(q_len * group / 256), a CTA pair's 512
-  int32_t box_slots;               // slots per TMA box (prefill_box_slots)
+  int32_t m_tiles;                 // ceil(q_len * group / kPrefillRowsPerCta)
   float scale_log2;                // softmax scale * log2(e)
   __nv_bfloat16* out;              // num_splits == 1: [tokens, Hq, 128]
   float* lse_out;                  // num_splits == 1: optional [tokens, Hq]
@@ -42,14 +40,9 @@ struct PrefillArgs {
 // Shared-memory bytes one CTA of the kernel takes (one CTA per SM).
 int prefill_smem_bytes();
 
-// Slots per TMA box: the largest power of two dividing block_size, at most
-// 128 (a single CTA's key tile) or 64 (a CTA pair's half of it).
-int prefill_box_slots(int block_size, bool pair);
-
-// Tensor maps: 5-D cache views with a box of (64 dims, prefill_box_slots
-// slots, 1 half, 1 head, 1 block).  pair: clusters of two CTAs, each row unit
-// 512 rows (m_tiles counts those); else one CTA per 256 rows.
+// Tensor maps: 5-D cache views with a box of (64 dims, b slots, 1 half, 1 head,
+// 1 block), b = the largest power of two dividing block_size, at most 128.
 cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const PrefillArgs& a, bool pair, cudaStream_t stream);
+                                 const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace pkvqk

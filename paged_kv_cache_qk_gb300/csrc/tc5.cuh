@@ -157,60 +157,5 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       : "memory");
 }
 
-// ------------------------------------------------- CTA pairs (cta_group::2)
-//
-// A pair of CTAs (cluster ranks 0 and 1) shares one MMA of M = 256 rows: rank 0
-// issues it; each CTA supplies its 128 rows of A from its own shared (or
-// tensor) memory and half of B's N columns from its own shared memory, at the
-// same offsets in both; each CTA's tensor memory receives its 128 rows of D.
-// A kernel uses either these forms or the cta_group::1 ones above, never both.
-
-// Both CTAs of the pair call these (one warp each), collectively.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D (+)= A (shared, desc) x B (shared, desc) over the pair; one thread of rank 0.
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D (+)= A (tensor memory) x B (shared, desc) over the pair; one thread of rank 0.
-__device__ __forceinline__ void mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at this shared-memory offset in every CTA of
-// `cta_mask` (bit r = cluster rank r) when every pair MMA this thread issued
-// so far has completed.
-__device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
-      "h"(cta_mask)
-      : "memory");
-}
-
 }  // namespace tc5
 }  // namespace pkvqk

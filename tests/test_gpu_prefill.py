@@ -63,10 +63,9 @@ CASES = [
     (16, 8, 50, 48, [61, 190]),
     (16, 8, 5, 16, [2000, 17, 0]),
     (16, 8, 1, 16, [900, 0, 31]),
-    # above 256 rows per kv head the CTA-pair form (512-row units): a last unit
-    # without tile B whose rank-1 CTA holds no rows (600 rows, pages of 256:
-    # 64-slot boxes; 580 rows, pages of 48), GQA 8 (800 rows, tile B of the
-    # last unit on rank 0 only), GQA 1 with a fresh 700-token prompt
+    # several CTAs per kv head with a ragged last one: without tile B (600 rows,
+    # pages of 256; 580 rows, pages of 48), GQA 8 (800 rows, a 32-row tile B),
+    # GQA 1 with a fresh 700-token prompt
     (16, 8, 300, 256, [300, 5]),
     (16, 8, 290, 48, [61, 190]),
     (32, 4, 100, 32, [250, 1]),
@@ -92,8 +91,8 @@ def test_prefill_splits_match_oracle(lib, S):
 
 
 @pytest.mark.parametrize("S", [2, 5])
-def test_prefill_pair_splits_match_oracle(lib, S):
-    # the CTA-pair form (600 rows per kv head) over split key ranges
+def test_prefill_many_row_tiles_splits_match_oracle(lib, S):
+    # 600 rows per kv head (three CTAs, the last one ragged) over split key ranges
     p = _problem(16, 8, 300, 16, [1500, 40, 0, 777], seed=41 + S)
     out, lse = _prefill(lib, p, num_splits=S)
     _check_all(p, out, lse, f"prefill pair S={S}")
