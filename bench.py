@@ -2,10 +2,13 @@
 """Benchmark of the paged decode-attention step on GB300.
 
 One step = the whole hot path over one batch: fused per-head RMSNorm + neox
-RoPE on q/k with the k/v append (pkvqk_norm_rope_append), split-KV paged
-decode attention (pkvqk_paged_decode) and, when the split count is above 1
-or the schedule is the balanced one, the LSE combine kernel it launches — all
-through the C ABI.
+RoPE on q/k with the k/v append (pkvqk_norm_rope_append_cached: the rotary
+sin/cos of each position come from a table that pkvqk_rope_table_build fills
+once per model, for Qwen3's 40960-position context, outside every timed
+region; the results are bit-identical to pkvqk_norm_rope_append's), split-KV
+paged decode attention (pkvqk_paged_decode) and, when the split count is
+above 1 or the schedule is the balanced one, the LSE combine kernel it
+launches — all through the C ABI.
 
 Default workload: Qwen3-0.6B decode, 16 q / 8 kv heads, head_dim 128, bf16,
 block_size 16, batch 64 x context 8192, shuffled block ids (2.15 GB of K/V
@@ -55,6 +58,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak) and seq-steps/s vs batch×ctx"
 NOMINAL_HBM_GBS = 8000.0
+ROPE_TABLE_POSITIONS = 40960          # Qwen3-0.6B's longest context
 FALLBACK_HBM_GBS = 6800.0
 
 WORKLOADS = {
@@ -627,6 +631,13 @@ class StepRunner:
         self.l2_bytes = l2_bytes
         self.big_inputs = self.decode_bytes > 4 * l2_bytes
         self.flush = flush
+        # the rotary table: model state built once (the longest context of
+        # Qwen3-0.6B, or further if a workload's positions go further)
+        self.table_positions = max(ROPE_TABLE_POSITIONS, int(p.positions.max().item()) + 1)
+        self.rope_table = torch.empty(lib.rope_table_bytes(self.table_positions),
+                                      dtype=torch.uint8, device=dev)
+        lib.rope_table_build(self.rope_table, self.table_positions, p.theta, stream=stream)
+        torch.cuda.synchronize()
 
     def cold_l2(self):
         # write 2x L2 (evicts every input line), then read another 2x L2 so
@@ -655,8 +666,10 @@ class StepRunner:
         p, stream = self.p, self.stream
         if ev is not None:
             ev[0].record(stream)
-        self.lib.norm_rope_append(self.q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q,
-                                  p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache, stream=stream)
+        self.lib.norm_rope_append_cached(self.q, p.k, p.v, p.positions, p.slot_mapping,
+                                         p.gamma_q, p.gamma_k, p.theta, p.eps, p.k_cache,
+                                         p.v_cache, self.rope_table, self.table_positions,
+                                         stream=stream)
         if ev is not None:
             ev[1].record(stream)
         self.decode_call(self.q, p.block_tables, p.seq_lens)
@@ -755,9 +768,10 @@ class StepRunner:
             stream.wait_event(uploaded[k])
             stream.wait_event(read_back[k])          # step i - 2's output has left outs[k]
             d = dev_ins[k]
-            lib.norm_rope_append(d["q"], d["k"], d["v"], d["positions"], d["slot_mapping"],
-                                 p.gamma_q, p.gamma_k, p.theta, p.eps, p.k_cache, p.v_cache,
-                                 stream=stream)
+            lib.norm_rope_append_cached(d["q"], d["k"], d["v"], d["positions"],
+                                        d["slot_mapping"], p.gamma_q, p.gamma_k, p.theta, p.eps,
+                                        p.k_cache, p.v_cache, self.rope_table,
+                                        self.table_positions, stream=stream)
             self.decode_call(d["q"], d["block_tables"], d["seq_lens"], d.get("cu_seqlens"),
                              outs[k])
             computed[k].record(stream)
@@ -917,6 +931,7 @@ def main():
                   "L2 flushed before every step (2x L2 written, then 2x L2 read so the "
                   "written lines are back in HBM before the step), excluded from timing",
             "parallelism": f"replicas x{world}",
+            "rope_table_positions": run.table_positions,
         },
         "seq_steps_per_s": round(aggregate_rate(world, p.B, ms), 1),
         "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),

@@ -140,6 +140,49 @@ PKVQK_API pkvqk_status pkvqk_norm_rope_append(
     int32_t* status_flags, pkvqk_stream_t stream);
 
 /*
+ * Bytes of a rotary table for positions 0 .. max_positions-1: 1 KiB per
+ * position.  0 when max_positions is outside 1 .. 2^21.
+ */
+PKVQK_API size_t pkvqk_rope_table_bytes(int32_t max_positions);
+
+/*
+ * Fills `table` with the rotary sin/cos that pkvqk_norm_rope_append computes
+ * for a token at each position p < max_positions (same source, item 2): for
+ * i < D/2 the angle p * theta^(-2i/D), reduced and evaluated exactly as that
+ * call does, kept as float-float pairs.  Build once per model (theta and the
+ * longest context), before the steps that read it; the table depends on
+ * nothing else.
+ *
+ *   table          device, 16-byte aligned, pkvqk_rope_table_bytes(max_positions)
+ *                  bytes, owned by the caller; written by a kernel on `stream`
+ *   max_positions  0 .. 2^21 (0: nothing to do)
+ * Errors: PKVQK_ERR_INVALID_ARG (max_positions out of range, theta not > 0,
+ * table not a 16-byte aligned device pointer).
+ */
+PKVQK_API pkvqk_status pkvqk_rope_table_build(void* table, int32_t max_positions, float theta,
+                                              pkvqk_stream_t stream);
+
+/*
+ * pkvqk_norm_rope_append with the angles of tokens at positions
+ * 0 .. table_positions-1 read from a table built by pkvqk_rope_table_build
+ * (with the same theta) instead of computed per token.  Tokens at other
+ * positions compute theirs as pkvqk_norm_rope_append does.  The results are
+ * bit-identical to pkvqk_norm_rope_append's.  Every other argument and error
+ * as there; table_positions 0 .. 2^21 (0: no table is read).
+ */
+PKVQK_API pkvqk_status pkvqk_norm_rope_append_cached(
+    void* q, int64_t q_stride_t, int64_t q_stride_h,
+    const void* k, int64_t k_stride_t, int64_t k_stride_h,
+    const void* v, int64_t v_stride_t, int64_t v_stride_h,
+    const int64_t* positions, const int64_t* slot_mapping,
+    const void* gamma_q, const void* gamma_k,
+    float theta, float eps,
+    int32_t num_tokens, int32_t num_q_heads,
+    void* k_cache, void* v_cache, const pkvqk_cache_layout* layout,
+    const void* rope_table, int32_t table_positions,
+    int32_t* status_flags, pkvqk_stream_t stream);
+
+/*
  * Schedule for pkvqk_paged_decode from host-side facts only (no device
  * read): batch, kv heads, rows per kv head (q_len * Hq/Hkv), the longest
  * sequence, the total key count and the SM count (0 = query the current

@@ -73,6 +73,19 @@ pkvqk_norm_rope_append = _sig("pkvqk_norm_rope_append", ctypes.c_int, [
     c_i32, c_i32,                       # num_tokens, num_q_heads
     c_vp, c_vp, ctypes.POINTER(CacheLayout),
     c_vp, c_vp])                        # status_flags, stream
+pkvqk_rope_table_bytes = _sig("pkvqk_rope_table_bytes", c_size, [c_i32])
+pkvqk_rope_table_build = _sig("pkvqk_rope_table_build", ctypes.c_int, [c_vp, c_i32, c_f32, c_vp])
+pkvqk_norm_rope_append_cached = _sig("pkvqk_norm_rope_append_cached", ctypes.c_int, [
+    c_vp, c_i64, c_i64,                 # q, strides
+    c_vp, c_i64, c_i64,                 # k
+    c_vp, c_i64, c_i64,                 # v
+    c_vp, c_vp,                         # positions, slot_mapping
+    c_vp, c_vp,                         # gamma_q, gamma_k
+    c_f32, c_f32,                       # theta, eps
+    c_i32, c_i32,                       # num_tokens, num_q_heads
+    c_vp, c_vp, ctypes.POINTER(CacheLayout),
+    c_vp, c_i32,                        # rope_table, table_positions
+    c_vp, c_vp])                        # status_flags, stream
 pkvqk_choose_num_splits = _sig("pkvqk_choose_num_splits", c_i32,
                                [c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_i32])
 pkvqk_decode_workspace_bytes = _sig("pkvqk_decode_workspace_bytes", c_size,
@@ -115,6 +128,7 @@ EXPORTED = [
     "pkvqk_paged_decode_partials", "pkvqk_lse_combine", "pkvqk_paged_decode_static_ws",
     "pkvqk_static_workspace_capacity", "pkvqk_choose_prefill_splits",
     "pkvqk_prefill_workspace_bytes", "pkvqk_paged_prefill", "pkvqk_paged_prefill_varlen",
+    "pkvqk_rope_table_bytes", "pkvqk_rope_table_build", "pkvqk_norm_rope_append_cached",
 ]
 
 
@@ -171,6 +185,37 @@ def norm_rope_append(q, k, v, positions, slot_mapping, gamma_q, gamma_k, theta, 
         _ptr(positions), _ptr(slot_mapping), _ptr(gamma_q), _ptr(gamma_k),
         float(theta), float(eps), T, Hq,
         _ptr(k_cache), _ptr(v_cache), ctypes.byref(lay),
+        _ptr(status_flags), _stream(stream)))
+
+
+def rope_table_bytes(max_positions):
+    return int(pkvqk_rope_table_bytes(max_positions))
+
+
+def rope_table_build(table, max_positions, theta, stream=None):
+    """table: device tensor of at least rope_table_bytes(max_positions) bytes."""
+    if max_positions > 0 and table.numel() * table.element_size() < rope_table_bytes(max_positions):
+        raise ValueError("rope table too small")
+    check(pkvqk_rope_table_build(_ptr(table), max_positions, float(theta), _stream(stream)))
+
+
+def norm_rope_append_cached(q, k, v, positions, slot_mapping, gamma_q, gamma_k, theta, eps,
+                            k_cache, v_cache, rope_table, table_positions, status_flags=None,
+                            stream=None):
+    """norm_rope_append with the angles of positions < table_positions read from a
+    table built by rope_table_build (same theta)."""
+    T, Hq, D = q.shape
+    lay = cache_layout(k_cache)
+    if tuple(v_cache.stride()) != tuple(k_cache.stride()) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must share one layout")
+    check(pkvqk_norm_rope_append_cached(
+        _ptr(q), q.stride(0), q.stride(1),
+        _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1),
+        _ptr(positions), _ptr(slot_mapping), _ptr(gamma_q), _ptr(gamma_k),
+        float(theta), float(eps), T, Hq,
+        _ptr(k_cache), _ptr(v_cache), ctypes.byref(lay),
+        _ptr(rope_table), int(table_positions),
         _ptr(status_flags), _stream(stream)))
 
 

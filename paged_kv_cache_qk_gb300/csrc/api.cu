@@ -161,6 +161,11 @@ int sm_count_current() {
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// Rotary table: per position, 16 lanes x 4 float4s (cos hi, cos lo, sin hi,
+// sin lo of four frequencies) = 1 KiB; up to 2^21 positions (2 GiB).
+constexpr size_t kRopeTableRowBytes = 16 * 4 * 16;
+constexpr int32_t kRopeTableMaxPositions = 1 << 21;
+
 // Split schedule: fp32 partials [rows][S][128], then partial lse [rows][S].
 size_t partial_bytes(int64_t rows, int S) {
   const size_t raw = static_cast<size_t>(rows) * S * (128 + 1) * sizeof(float);
@@ -462,15 +467,25 @@ const char* pkvqk_last_error(void) { return g_last_error.c_str(); }
 
 int32_t pkvqk_abi_version(void) { return 1; }
 
-pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_stride_h,
-                                    const void* k, int64_t k_stride_t, int64_t k_stride_h,
-                                    const void* v, int64_t v_stride_t, int64_t v_stride_h,
-                                    const int64_t* positions, const int64_t* slot_mapping,
-                                    const void* gamma_q, const void* gamma_k, float theta,
-                                    float eps, int32_t num_tokens, int32_t num_q_heads,
-                                    void* k_cache, void* v_cache,
-                                    const pkvqk_cache_layout* layout, int32_t* status_flags,
-                                    pkvqk_stream_t stream) {
+namespace {
+
+// theta^(-2i/D) in float64 and the float-float sin/cos knots: the inputs of
+// both the append kernel's angle phase and the table build.
+void rope_constants(float theta, double (&inv_freq)[64], float (&tab)[pkvqk::kSinCosKnots][4]) {
+  for (int i = 0; i < 64; ++i) inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
+  static float s_tab[pkvqk::kSinCosKnots][4];
+  static std::once_flag s_tab_once;
+  std::call_once(s_tab_once, [] { pkvqk::build_sincos_table(s_tab); });
+  std::memcpy(tab, s_tab, sizeof(s_tab));
+}
+
+pkvqk_status run_append(void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                        int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                        int64_t v_stride_h, const int64_t* positions, const int64_t* slot_mapping,
+                        const void* gamma_q, const void* gamma_k, float theta, float eps,
+                        int32_t num_tokens, int32_t num_q_heads, void* k_cache, void* v_cache,
+                        const pkvqk_cache_layout* layout, const void* rope_table,
+                        int32_t table_positions, int32_t* status_flags, pkvqk_stream_t stream) {
   PKVQK_TRY(check_layout(layout));
   const pkvqk_cache_layout& L = *layout;
   if (num_tokens < 0 || num_tokens > (1 << 30))
@@ -499,6 +514,10 @@ pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_strid
     if (!aligned16(al[i])) return fail(PKVQK_ERR_INVALID_ARG, "bf16 base pointer not 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(positions) & 7u) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return fail(PKVQK_ERR_INVALID_ARG, "positions/slot_mapping not 8-byte aligned");
+  if (table_positions > 0) {
+    PKVQK_TRY(check_device_ptr(rope_table, "rope_table"));
+    if (!aligned16(rope_table)) return fail(PKVQK_ERR_INVALID_ARG, "rope_table not 16-byte aligned");
+  }
 
   pkvqk::NormRopeAppendArgs a;
   a.q = static_cast<__nv_bfloat16*>(q);
@@ -515,12 +534,7 @@ pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_strid
   a.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
   a.gamma_k = static_cast<const __nv_bfloat16*>(gamma_k);
   a.eps = eps;
-  for (int i = 0; i < 64; ++i)
-    a.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
-  static float s_tab[pkvqk::kSinCosKnots][4];
-  static std::once_flag s_tab_once;
-  std::call_once(s_tab_once, [] { pkvqk::build_sincos_table(s_tab); });
-  std::memcpy(a.sincos_tab, s_tab, sizeof(s_tab));
+  rope_constants(theta, a.inv_freq, a.sincos_tab);
   a.num_tokens = num_tokens;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = L.num_kv_heads;
@@ -532,8 +546,66 @@ pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_strid
   a.slot_stride = L.slot_stride;
   a.head_stride = L.head_stride;
   a.status_flags = status_flags;
+  a.rope_table = table_positions > 0 ? static_cast<const float4*>(rope_table) : nullptr;
+  a.table_positions = table_positions > 0 ? table_positions : 0;
   cudaError_t e = pkvqk::launch_norm_rope_append(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "norm_rope_append launch");
+  return ok();
+}
+
+}  // namespace
+
+pkvqk_status pkvqk_norm_rope_append(void* q, int64_t q_stride_t, int64_t q_stride_h,
+                                    const void* k, int64_t k_stride_t, int64_t k_stride_h,
+                                    const void* v, int64_t v_stride_t, int64_t v_stride_h,
+                                    const int64_t* positions, const int64_t* slot_mapping,
+                                    const void* gamma_q, const void* gamma_k, float theta,
+                                    float eps, int32_t num_tokens, int32_t num_q_heads,
+                                    void* k_cache, void* v_cache,
+                                    const pkvqk_cache_layout* layout, int32_t* status_flags,
+                                    pkvqk_stream_t stream) {
+  return run_append(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t,
+                    v_stride_h, positions, slot_mapping, gamma_q, gamma_k, theta, eps, num_tokens,
+                    num_q_heads, k_cache, v_cache, layout, nullptr, 0, status_flags, stream);
+}
+
+pkvqk_status pkvqk_norm_rope_append_cached(
+    void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k, int64_t k_stride_t,
+    int64_t k_stride_h, const void* v, int64_t v_stride_t, int64_t v_stride_h,
+    const int64_t* positions, const int64_t* slot_mapping, const void* gamma_q,
+    const void* gamma_k, float theta, float eps, int32_t num_tokens, int32_t num_q_heads,
+    void* k_cache, void* v_cache, const pkvqk_cache_layout* layout, const void* rope_table,
+    int32_t table_positions, int32_t* status_flags, pkvqk_stream_t stream) {
+  if (table_positions < 0 || table_positions > kRopeTableMaxPositions)
+    return fail(PKVQK_ERR_INVALID_ARG, "table_positions %d (0..%d)", table_positions,
+                kRopeTableMaxPositions);
+  return run_append(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t,
+                    v_stride_h, positions, slot_mapping, gamma_q, gamma_k, theta, eps, num_tokens,
+                    num_q_heads, k_cache, v_cache, layout, rope_table, table_positions,
+                    status_flags, stream);
+}
+
+size_t pkvqk_rope_table_bytes(int32_t max_positions) {
+  if (max_positions <= 0 || max_positions > kRopeTableMaxPositions) return 0;
+  return static_cast<size_t>(max_positions) * kRopeTableRowBytes;
+}
+
+pkvqk_status pkvqk_rope_table_build(void* table, int32_t max_positions, float theta,
+                                    pkvqk_stream_t stream) {
+  if (max_positions < 0 || max_positions > kRopeTableMaxPositions)
+    return fail(PKVQK_ERR_INVALID_ARG, "max_positions %d (0..%d)", max_positions,
+                kRopeTableMaxPositions);
+  if (!(theta > 0.f) || !std::isfinite(theta)) return fail(PKVQK_ERR_INVALID_ARG, "theta must be > 0");
+  if (max_positions == 0) return ok();
+  PKVQK_TRY(check_device_ptr(table, "table"));
+  if (!aligned16(table)) return fail(PKVQK_ERR_INVALID_ARG, "table not 16-byte aligned");
+  double inv_freq[64];
+  float tab[pkvqk::kSinCosKnots][4];
+  rope_constants(theta, inv_freq, tab);
+  const cudaError_t e = pkvqk::launch_rope_table_build(
+      static_cast<float4*>(table), max_positions, inv_freq, tab,
+      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope table build launch");
   return ok();
 }
 

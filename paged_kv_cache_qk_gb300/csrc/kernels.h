@@ -30,9 +30,19 @@ struct NormRopeAppendArgs {
   int32_t block_size;
   int64_t block_stride, slot_stride, head_stride;
   int32_t* status_flags;
+  // optional: sin/cos of positions 0 .. table_positions-1 from
+  // launch_rope_table_build (nullptr / 0: every token computes its own)
+  const float4* rope_table;
+  int32_t table_positions;
 };
 
 cudaError_t launch_norm_rope_append(const NormRopeAppendArgs& a, cudaStream_t stream);
+
+// Fills table[pos][l][4] (l < 16: float4s cos_hi, cos_lo, sin_hi, sin_lo of
+// frequencies 4l .. 4l+3) for pos < positions with the values the append
+// kernel computes for a token at pos.
+cudaError_t launch_rope_table_build(float4* table, int32_t positions, const double (&inv_freq)[64],
+                                    const float (&sincos_tab)[51][4], cudaStream_t stream);
 
 struct DecodeArgs {
   const __nv_bfloat16* q;

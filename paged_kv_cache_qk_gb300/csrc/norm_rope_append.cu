@@ -29,6 +29,13 @@
 // (decode): one half-warp per vector, the shortest path per token.  Many
 // tokens (prefill chunks): three or more warps per token and up to four
 // vectors per half-warp, so several tokens per SM overlap their latencies.
+//
+// The angles depend on the position alone, so a caller may build them once
+// (launch_rope_table_build: the same float64 reduction and float-float sin/cos,
+// kept per position as the float4s a lane reads) and pass the table: a token
+// whose position is in it loads its lane's 64 bytes with the q/k/v loads and
+// skips the angle phase; any other token computes its angles as above.  Both
+// ways give the same bits.
 #include "device_common.cuh"
 #include "kernels.h"
 #include "rope_math.cuh"
@@ -46,6 +53,10 @@ constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
 // 10 at 64 registers with spills 53.4 us).
 constexpr int kManyThreads = 96;
 constexpr int kManyMinBlocks = 8;
+// With the angles from a table, 10 CTAs per SM at 64 registers (a few bytes
+// of spill, in the per-token angle fallback): 8192 tokens 34.0 us at 8 per
+// SM, 32.2 at 9, 31.0 at 10, 33.8 at 11 (measured on GB300).
+constexpr int kTableMinBlocks = 10;
 
 // A lane's part of one head vector: elements [4l, 4l + 4) and their
 // rotate-half partners [64 + 4l, 64 + 4l + 4), as raw bf16 (x, and v for kv
@@ -150,7 +161,41 @@ __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t
   }
 }
 
-template <int kThreadsBound, int kMinBlocks>
+// The token's sin/cos through shared memory: the knots copied in, 64 angles
+// (one per lane of warps 0 and 1: every lane of a float64 instruction busy),
+// float64 angle and quarter-turn reduction, float-float sin/cos.  CTA-wide.
+__device__ __forceinline__ Trig angles_in_cta(const NormRopeAppendArgs& a, int64_t pos, int l,
+                                              float (*s_tab)[4], float* s_cos_hi,
+                                              float* s_cos_lo, float* s_sin_hi,
+                                              float* s_sin_lo) {
+  // the sin/cos knots to shared memory: the lookups below take a different
+  // knot in every lane, and indexing the parameter copy that way costs one
+  // constant-cache access per distinct address (cold misses included) on the
+  // angle's critical path
+  for (int e = threadIdx.x; e < kSinCosKnots * 4; e += blockDim.x)
+    (&s_tab[0][0])[e] = (&a.sincos_tab[0][0])[e];
+  __syncthreads();
+  if (threadIdx.x < kHeadDim / 2) {
+    const int i = threadIdx.x;
+    FF x, sn, cs;
+    const int quadrant = reduce_angle(static_cast<double>(pos), a.inv_freq[i], &x);
+    sincos_ff(x, quadrant, s_tab, &sn, &cs);
+    s_cos_hi[i] = cs.hi;
+    s_cos_lo[i] = cs.lo;
+    s_sin_hi[i] = sn.hi;
+    s_sin_lo[i] = sn.lo;
+  }
+  __syncthreads();
+  // this lane's four frequencies, for every head vector it finishes
+  Trig tr;
+  tr.ch = *reinterpret_cast<const float4*>(s_cos_hi + 4 * l);
+  tr.cl = *reinterpret_cast<const float4*>(s_cos_lo + 4 * l);
+  tr.sh = *reinterpret_cast<const float4*>(s_sin_hi + 4 * l);
+  tr.sl = *reinterpret_cast<const float4*>(s_sin_lo + 4 * l);
+  return tr;
+}
+
+template <int kThreadsBound, int kMinBlocks, bool kTable>
 __global__ void __launch_bounds__(kThreadsBound, kMinBlocks)
 norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   __shared__ __align__(16) float s_cos_hi[kHeadDim / 2], s_cos_lo[kHeadDim / 2];
@@ -180,26 +225,17 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
                        __ldg(reinterpret_cast<const uint2*>(a.gamma_q + 64 + 4 * l))};
   const uint2 gk[2] = {__ldg(reinterpret_cast<const uint2*>(a.gamma_k + 4 * l)),
                        __ldg(reinterpret_cast<const uint2*>(a.gamma_k + 64 + 4 * l))};
-  // the sin/cos knots to shared memory while those loads are in flight: the
-  // lookups below take a different knot in every lane, and indexing the
-  // parameter copy that way costs one constant-cache access per distinct
-  // address (cold misses included) on the angle's critical path
-  for (int e = threadIdx.x; e < kSinCosKnots * 4; e += blockDim.x)
-    (&s_tab[0][0])[e] = (&a.sincos_tab[0][0])[e];
-  __syncthreads();
-
-  // the token's 64 angles, one per lane of warps 0 and 1 (every lane of a
-  // float64 instruction busy): float64 angle and quarter-turn reduction,
-  // float-float sin/cos
-  if (warp < 2) {
-    const int i = threadIdx.x;
-    FF x, sn, cs;
-    const int quadrant = reduce_angle(static_cast<double>(pos), a.inv_freq[i], &x);
-    sincos_ff(x, quadrant, s_tab, &sn, &cs);
-    s_cos_hi[i] = cs.hi;
-    s_cos_lo[i] = cs.lo;
-    s_sin_hi[i] = sn.hi;
-    s_sin_lo[i] = sn.lo;
+  // uniform over the CTA (one token)
+  const bool from_table = kTable && pos >= 0 && pos < a.table_positions;
+  Trig tr;
+  if (from_table) {
+    const float4* row = a.rope_table + (pos * (kHeadDim / 8) + l) * 4;
+    tr.ch = __ldg(row);
+    tr.cl = __ldg(row + 1);
+    tr.sh = __ldg(row + 2);
+    tr.sl = __ldg(row + 3);
+  } else {
+    tr = angles_in_cta(a, pos, l, s_tab, s_cos_hi, s_cos_lo, s_sin_hi, s_sin_lo);
   }
   const int64_t nslots = a.num_blocks * static_cast<int64_t>(a.block_size);
   if (threadIdx.x == 0 && slot >= nslots) report(a.status_flags, kFlagBadSlot);
@@ -207,13 +243,6 @@ norm_rope_append_kernel(const __grid_constant__ NormRopeAppendArgs a) {
   const int64_t blk = write_cache ? slot / a.block_size : 0;
   const int64_t off = write_cache ? slot % a.block_size : 0;
   const int64_t cache_row = blk * a.block_stride + off * a.slot_stride;
-  __syncthreads();
-  // this lane's four frequencies, for every head vector it finishes
-  Trig tr;
-  tr.ch = *reinterpret_cast<const float4*>(s_cos_hi + 4 * l);
-  tr.cl = *reinterpret_cast<const float4*>(s_cos_lo + 4 * l);
-  tr.sh = *reinterpret_cast<const float4*>(s_sin_hi + 4 * l);
-  tr.sl = *reinterpret_cast<const float4*>(s_sin_lo + 4 * l);
 
   // warp-uniform: both half-warps of a warp share `base`
   const int num_vec = a.num_q_heads + a.num_kv_heads;
@@ -242,11 +271,57 @@ cudaError_t launch_norm_rope_append(const NormRopeAppendArgs& a, cudaStream_t st
   const int per_half_warp = many ? kHoist : 1;
   int warps = (num_vec + 2 * per_half_warp - 1) / (2 * per_half_warp);
   warps = warps < 2 ? 2 : (warps > kMaxThreads / 32 ? kMaxThreads / 32 : warps);
+  const bool table = a.rope_table != nullptr && a.table_positions > 0;
   if (many && warps * 32 <= kManyThreads)
-    return launch_pdl(norm_rope_append_kernel<kManyThreads, kManyMinBlocks>, dim3(a.num_tokens),
-                      dim3(warps * 32), 0, stream, a);
-  return launch_pdl(norm_rope_append_kernel<kMaxThreads, 1>, dim3(a.num_tokens), dim3(warps * 32),
-                    0, stream, a);
+    return launch_pdl(table ? norm_rope_append_kernel<kManyThreads, kTableMinBlocks, true>
+                            : norm_rope_append_kernel<kManyThreads, kManyMinBlocks, false>,
+                      dim3(a.num_tokens), dim3(warps * 32), 0, stream, a);
+  return launch_pdl(table ? norm_rope_append_kernel<kMaxThreads, 1, true>
+                          : norm_rope_append_kernel<kMaxThreads, 1, false>,
+                    dim3(a.num_tokens), dim3(warps * 32), 0, stream, a);
+}
+
+namespace {
+
+struct RopeTableArgs {
+  float4* table;
+  int32_t positions;
+  double inv_freq[64];
+  float sincos_tab[kSinCosKnots][4];
+};
+
+// One CTA per position, thread i = frequency i: the same steps as the append
+// kernel's angle phase, stored where lane i/4 of a half-warp reads them.
+__global__ void __launch_bounds__(64) rope_table_kernel(const __grid_constant__ RopeTableArgs a) {
+  __shared__ float s_tab[kSinCosKnots][4];
+  for (int e = threadIdx.x; e < kSinCosKnots * 4; e += blockDim.x)
+    (&s_tab[0][0])[e] = (&a.sincos_tab[0][0])[e];
+  __syncthreads();
+  const int64_t pos = blockIdx.x;
+  const int i = threadIdx.x;
+  FF x, sn, cs;
+  const int quadrant = reduce_angle(static_cast<double>(pos), a.inv_freq[i], &x);
+  sincos_ff(x, quadrant, s_tab, &sn, &cs);
+  float* row = reinterpret_cast<float*>(a.table + (pos * (kHeadDim / 8) + i / 4) * 4);
+  row[0 * 4 + (i & 3)] = cs.hi;
+  row[1 * 4 + (i & 3)] = cs.lo;
+  row[2 * 4 + (i & 3)] = sn.hi;
+  row[3 * 4 + (i & 3)] = sn.lo;
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table_build(float4* table, int32_t positions, const double (&inv_freq)[64],
+                                    const float (&sincos_tab)[51][4], cudaStream_t stream) {
+  if (positions <= 0) return cudaSuccess;
+  RopeTableArgs a;
+  a.table = table;
+  a.positions = positions;
+  for (int i = 0; i < 64; ++i) a.inv_freq[i] = inv_freq[i];
+  for (int k = 0; k < kSinCosKnots; ++k)
+    for (int c = 0; c < 4; ++c) a.sincos_tab[k][c] = sincos_tab[k][c];
+  rope_table_kernel<<<positions, 64, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace pkvqk

@@ -183,3 +183,28 @@ def test_static_ws_reports_argument_errors_before_its_capacity(lib):
     # a valid call whose partials do not fit is refused before any launch
     assert call(B=4096, S=200) == lib.PKVQK_ERR_WORKSPACE_TOO_SMALL
     assert call(B=0, S=4) == lib.PKVQK_OK
+
+
+def test_rope_table_size_and_argument_errors(lib):
+    # 1 KiB per position (16 lanes x 4 float4s), nothing outside 1 .. 2^21
+    assert lib.rope_table_bytes(1) == 1024
+    assert lib.rope_table_bytes(40960) == 40960 * 1024
+    assert lib.rope_table_bytes(0) == 0 and lib.rope_table_bytes(-3) == 0
+    assert lib.rope_table_bytes((1 << 21) + 1) == 0
+    b = lib.pkvqk_rope_table_build
+    assert b(FAKE, -1, 1e6, None) == lib.PKVQK_ERR_INVALID_ARG
+    assert b(FAKE, (1 << 21) + 1, 1e6, None) == lib.PKVQK_ERR_INVALID_ARG
+    assert b(FAKE, 16, 0.0, None) == lib.PKVQK_ERR_INVALID_ARG
+    assert b(FAKE, 16, float("nan"), None) == lib.PKVQK_ERR_INVALID_ARG
+    assert b(FAKE, 0, 1e6, None) == lib.PKVQK_OK           # nothing to build
+    lay = _layout(lib)
+
+    def cached(table_positions, theta=1e6, T=4):
+        return lib.pkvqk_norm_rope_append_cached(FAKE, 2048, 128, FAKE, 1024, 128, FAKE, 1024,
+                                                 128, FAKE, FAKE, FAKE, FAKE, theta, 1e-6, T, 16,
+                                                 FAKE, FAKE, ctypes.byref(lay), FAKE,
+                                                 table_positions, None, None)
+    assert cached(-1) == lib.PKVQK_ERR_INVALID_ARG
+    assert cached((1 << 21) + 1) == lib.PKVQK_ERR_INVALID_ARG
+    assert cached(16, theta=0.0) == lib.PKVQK_ERR_INVALID_ARG  # the append's own checks follow
+    assert cached(16, T=0) == lib.PKVQK_OK

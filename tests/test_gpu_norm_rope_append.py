@@ -124,3 +124,70 @@ def test_zero_tokens_is_noop(lib):
                          p.gamma_q, p.gamma_k, p.theta, p.eps, kc, p.v_cache)
     torch.cuda.synchronize()
     assert torch.equal(kc, p.k_cache)
+
+
+def _append_both(lib, p, positions, table_positions, slots=None):
+    """The same inputs through pkvqk_norm_rope_append and, with a rotary table
+    of table_positions positions, pkvqk_norm_rope_append_cached."""
+    slots = p.slot_mapping if slots is None else slots
+    table = torch.empty(max(lib.rope_table_bytes(table_positions), 16), dtype=torch.uint8,
+                        device="cuda")
+    lib.rope_table_build(table, table_positions, p.theta)
+    outs = []
+    for cached in (False, True):
+        q, kc, vc = p.q.clone(), p.k_cache.clone(), p.v_cache.clone()
+        flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if cached:
+            lib.norm_rope_append_cached(q, p.k, p.v, positions, slots, p.gamma_q, p.gamma_k,
+                                        p.theta, p.eps, kc, vc, table, table_positions,
+                                        status_flags=flags)
+        else:
+            lib.norm_rope_append(q, p.k, p.v, positions, slots, p.gamma_q, p.gamma_k, p.theta,
+                                 p.eps, kc, vc, status_flags=flags)
+        torch.cuda.synchronize()
+        outs.append((q, kc, vc, flags.item()))
+    return outs
+
+
+@pytest.mark.parametrize("T", [5, 2048])
+def test_rope_table_gives_the_same_bits(lib, T):
+    """Angles from the table are the ones the kernel computes per token: q, the
+    cache and the flags are bit-identical, for positions inside the table, past
+    its end (computed per token) and at its edges; few tokens (one half-warp per
+    vector) and many (the narrow-CTA form)."""
+    Hq, Hkv, D, bs, NB = 16, 8, 128, 16, 160
+    g = torch.Generator(device="cuda").manual_seed(931 + T)
+    p = workloads.make_problem("table", Hq, Hkv, D, bs, [1], 1, NB, 931, "cuda")
+    p.q = torch.randn(T, Hq, D, generator=g, device="cuda").to(torch.bfloat16)
+    p.k = torch.randn(T, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    p.v = torch.randn(T, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    P = 40960
+    pos = torch.randint(0, 65536, (T,), generator=g, device="cuda")
+    edges = torch.tensor([0, 1, P - 1, P, P + 1, 65535, 32767], device="cuda")
+    pos[:min(T, edges.numel())] = edges[:min(T, edges.numel())]
+    slots = torch.full((T,), -1, dtype=torch.int64, device="cuda")
+    n = min(T, NB * bs)
+    slots[:n] = torch.randperm(NB * bs, generator=g, device="cuda")[:n]
+    (q0, k0, v0, f0), (q1, k1, v1, f1) = _append_both(lib, p, pos, P, slots)
+    assert torch.equal(bits_t(q0), bits_t(q1))
+    assert torch.equal(bits_t(k0), bits_t(k1)) and torch.equal(bits_t(v0), bits_t(v1))
+    assert f0 == f1 == 0
+
+
+def test_rope_table_path_matches_oracle(lib):
+    # the cached path against the fp64 oracle at the 1-ulp bar (verify tokens at
+    # positions up to ~8200, all inside a 16384-position table)
+    p = workloads.verify_causal(device="cuda")
+    (_, _, _, _), (q1, kc1, vc1, f1) = _append_both(lib, p, p.positions, 16384)
+    qh, kc, vc, _, _ = oracle.norm_rope_append(
+        bits(p.q), bits(p.k), bits(p.v), p.positions.cpu().numpy(),
+        p.slot_mapping.cpu().numpy(), bits(p.gamma_q), bits(p.gamma_k), p.theta, p.eps,
+        bits(p.k_cache), bits(p.v_cache), p.block_size)
+    assert bf16_ulp_distance(bits(q1), qh).max() <= ULP_TOL
+    assert bf16_ulp_distance(bits(kc1), kc).max() <= ULP_TOL
+    assert np.array_equal(bits(vc1), vc)
+    assert f1 == 0
+
+
+def bits_t(t):
+    return t.view(torch.int16)
