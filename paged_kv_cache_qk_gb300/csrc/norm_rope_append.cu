@@ -54,8 +54,9 @@ constexpr int kManyTokens = 1024;    // from here on, narrow CTAs
 constexpr int kManyThreads = 96;
 constexpr int kManyMinBlocks = 8;
 // With the angles from a table, 10 CTAs per SM at 64 registers (a few bytes
-// of spill, in the per-token angle fallback): 8192 tokens 34.0 us at 8 per
-// SM, 32.2 at 9, 31.0 at 10, 33.8 at 11 (measured on GB300).
+// of spill, in the per-token angle fallback): 8192 tokens with the scalar
+// rotation 34.0 us at 8 per SM, 32.2 at 9, 31.0 at 10, 33.8 at 11; with the
+// packed rotation 31.6 at 8, 31.1 at 9, 29.0 at 10 (measured on GB300).
 constexpr int kTableMinBlocks = 10;
 
 // A lane's part of one head vector: elements [4l, 4l + 4) and their
@@ -95,14 +96,27 @@ __device__ __forceinline__ Loaded load_vector(const NormRopeAppendArgs& a, int t
   return r;
 }
 
-// r * (a c - b s) for c = ch + cl, s = sh + sl: the products a*ch and b*sh
-// error-free (p + e), the low parts and the error terms added last.
-__device__ __forceinline__ float rotate(float a, float b, float ch, float cl, float sh, float sl,
-                                        float r) {
-  const float p1 = a * ch, e1 = fmaf(a, ch, -p1);   // a*c_hi = p1 + e1 exactly
-  const float p2 = -b * sh, e2 = fmaf(-b, sh, -p2); // -b*s_hi = p2 + e2 exactly
-  const float tail = fmaf(a, cl, -b * sl) + (e1 + e2);
-  return r * ((p1 + p2) + tail);
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// r * (a c - b s) for c = ch + cl, s = sh + sl, two elements at once (packed
+// f32x2, each lane rounded as the scalar instruction rounds it): the products
+// a*ch and b*sh error-free (p1 = a ch rounded, its error -(p1 - a ch) from
+// one fma against -ch; q2 = b sh rounded, the error of -b sh as q2 - b sh),
+// the low parts and the error terms added last.  nch, nsh, nsl are -ch, -sh,
+// -sl (exact), so no negation is spent per element.
+__device__ __forceinline__ uint64_t rotate2(uint64_t a, uint64_t b, uint64_t ch, uint64_t nch,
+                                            uint64_t cl, uint64_t sh, uint64_t nsh, uint64_t nsl,
+                                            uint64_t r) {
+  const uint64_t p1 = mul2(a, ch);
+  const uint64_t m1 = fma2(a, nch, p1);
+  const uint64_t q2 = mul2(b, sh);
+  const uint64_t e2 = fma2(b, nsh, q2);
+  const uint64_t tail = add2(fma2(a, cl, mul2(b, nsl)), sub2(e2, m1));
+  return mul2(r, add2(sub2(p1, q2), tail));
 }
 
 // Norm + rotation + stores of one head vector; both half-warps of the warp
@@ -137,11 +151,18 @@ __device__ __forceinline__ void finish_vector(const NormRopeAppendArgs& a, int t
   const float cl[4] = {tr.cl.x, tr.cl.y, tr.cl.z, tr.cl.w};
   const float sh[4] = {tr.sh.x, tr.sh.y, tr.sh.z, tr.sh.w};
   const float sl[4] = {tr.sl.x, tr.sl.y, tr.sl.z, tr.sl.w};
+  const uint64_t r2 = pack2(r, r);
   float o0[4], o1[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    o0[j] = rotate(a0[j], a1[j], ch[j], cl[j], sh[j], sl[j], r);
-    o1[j] = rotate(a1[j], -a0[j], ch[j], cl[j], sh[j], sl[j], r);
+  for (int j = 0; j < 4; j += 2) {
+    const uint64_t x0 = pack2(a0[j], a0[j + 1]), x1 = pack2(a1[j], a1[j + 1]);
+    const uint64_t c = pack2(ch[j], ch[j + 1]), nc = pack2(-ch[j], -ch[j + 1]);
+    const uint64_t c_lo = pack2(cl[j], cl[j + 1]);
+    const uint64_t s = pack2(sh[j], sh[j + 1]), ns = pack2(-sh[j], -sh[j + 1]);
+    const uint64_t s_lo = pack2(sl[j], sl[j + 1]), ns_lo = pack2(-sl[j], -sl[j + 1]);
+    // out_i = r (a_i c - a_{i+64} s);  out_{i+64} = r (a_{i+64} c - (-a_i) s)
+    unpack2(rotate2(x0, x1, c, nc, c_lo, s, ns, ns_lo, r2), o0[j], o0[j + 1]);
+    unpack2(rotate2(x1, x0, c, nc, c_lo, ns, s, s_lo, r2), o1[j], o1[j + 1]);
   }
   const uint2 w0 = make_uint2(pack_bf16x2(o0[0], o0[1]), pack_bf16x2(o0[2], o0[3]));
   const uint2 w1 = make_uint2(pack_bf16x2(o1[0], o1[1]), pack_bf16x2(o1[2], o1[3]));
