@@ -20,14 +20,16 @@
 // rings (K and V separately); both row tiles use every key tile, and the
 // tensor core alternates between them so that one tile's softmax runs while
 // the other tile's MMAs do (ping-pong).  Warp roles:
-//   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (tensor-memory
-//              lane r).  Reads its score row S = Q K^T from tensor memory,
-//              keeps the running max and sum, writes P (bf16 pairs) back into
-//              the first 64 columns of its own S buffer, rescales O in tensor
-//              memory only when the max grew by more than 2^8 (P <= 2^8
-//              otherwise), and writes the output row at the end;
-//   warp 8     TMA producer: one box per (page, 64-dim half) of K and of V;
-//   warp 9     allocates the tensor memory; lane 0 issues the MMAs in the
+//   warps 0-7 / 8-15  softmax of tile A / B, two threads per row: warp
+//              8x + 4h + q owns lanes 32q..32q+31 (rows) and keys 64h..64h+63
+//              of every key tile.  Reads its half of the score row S = Q K^T
+//              from tensor memory, keeps the running max and sum, writes P
+//              (bf16 pairs) back over the S columns it has read, swaps its
+//              reference max with the other half once per tile, rescales its
+//              half of O in tensor memory only when the max grew by more than
+//              2^8 (P <= 2^8 otherwise), and writes its 64 output dims;
+//   warp 16    TMA producer: one box per (page, 64-dim half) of K and of V;
+//   warp 17    allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
 //              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
 //                               operands in shared memory),
@@ -43,8 +45,9 @@
 //   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]      2 x 32 KiB
 //   K stage s [2 dim halves][128 keys][64 bf16]      2 x 32 KiB
 //   V stage s  the same                              2 x 32 KiB
-// Tensor memory: S_A (then P_A) at columns 0-127, S_B (P_B) 128-255, O_A
-// 256-383, O_B 384-511.
+//   pair-swap slots [tile][parity][half][128 rows] fp32  4 KiB
+// Tensor memory: S_A at columns 0-127 (P_A over columns 0-31 and 64-95), S_B
+// 128-255 (P_B likewise), O_A 256-383, O_B 384-511.
 //
 // Every wait is bounded: on a timeout the CTA reports PKVQK_FLAG_WAIT_TIMEOUT,
 // lets its own copies and MMAs in flight finish (bounded), frees its tensor
@@ -67,9 +70,10 @@ constexpr int kOffQ = 0;                       // Q_A, Q_B
 constexpr int kOffK = 2 * kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kDataBytes = kOffV + kStages * kTile;
-constexpr int kThreads = 10 * 32;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxWarps = 16;             // 8 per row tile, two per lane quadrant
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                  // + x * kN
 constexpr uint32_t kColO = 256;                // + x * kN
@@ -83,11 +87,14 @@ struct Bars {
   uint64_t p_full[2];                            // P_x written (and O_x rescaled)
   uint64_t pv_done[2];                           // the last O_x += P_x V finished
   uint64_t drain;                                // MMA thread's own completion (timeout path)
+  uint64_t xch[2][4];                            // warp pair (tile, lane quadrant) swaps
   uint32_t tmem_base;
   int32_t abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-constexpr int kSmemBytes = kDataBytes + 256 + 1024;   // + barriers + alignment slack
+constexpr int kOffSlots = kDataBytes + 256;   // pair-swap slots [tile][parity][half][row]
+constexpr int kSlotBytes = 2 * 2 * 2 * kM * 4;
+constexpr int kSmemBytes = kOffSlots + kSlotBytes + 1024;   // + alignment slack
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_addr(p);
@@ -278,11 +285,12 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     if (x == 0 && !mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
     const uint32_t vt = smem_addr(smem + kOffV + s * kTile);
-    // P_x: 16 keys per step = 8 columns of bf16 pairs
+    // P_x: 16 keys per step = 8 columns of bf16 pairs; keys 64h.. at column 64h
 #pragma unroll
     for (int ks = 0; ks < kN / 16; ++ks)
-      tc5::mma_f16_ts(tmem + kColO + x * kN, tmem + kColS + x * kN + ks * 8, desc_v(vt, ks),
-                      idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+      tc5::mma_f16_ts(tmem + kColO + x * kN,
+                      tmem + kColS + x * kN + (ks >> 2) * (kN / 2) + (ks & 3) * 8,
+                      desc_v(vt, ks), idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
     if (i == n - 1) tc5::commit(&bars->pv_done[x]);
     if (x == last) tc5::commit(&bars->empty_v[s]);
     return true;
@@ -307,6 +315,19 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
 }
 
 // --------------------------------------------------------------- softmax
+//
+// Two threads per row: the warp pair (tile x, lane quadrant q, half 0/1)
+// shares tensor-memory lanes 32q..32q+31, and half h owns keys 64h..64h+63 of
+// every key tile and dims 64h..64h+63 of O.  Each thread keeps a reference
+// max m_ref (log2 units, an integer once set) and writes P = 2^(s sl2 - m_ref)
+// as bf16 pairs over the S columns it has already read: half h's keys
+// 64h + 2j, +1 land in column 64h + j, which is where the PV MMA reads them.
+// A 32-key chunk's max is taken from registers before its exponentials; if
+// it exceeds m_ref by more than 2^8 the reference is raised to the ceiling of
+// that max first, so P <= 2^8 always, and P already written for the tile is
+// scaled by the (exact, power-of-two) ratio.  After the tile the two halves
+// swap their references and the lower one scales its P the same way, so both
+// use one reference for the row; O is rescaled only when that reference rose.
 
 // 2^x on the SFU (relative error ~2^-22; -inf -> +0).  P is rounded to bf16
 // right after, so the approximate unit is accurate enough.
@@ -322,75 +343,108 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Max of the visible scores (keys e < nvis of the tile) of this thread's row
-// of the S buffer at taddr, read 32 columns at a time; four independent
-// three-input chains.
-template <bool kMasked>
-__device__ __forceinline__ float tile_max(uint32_t taddr, int nvis) {
-  float m[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) m[j] = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < kN / 32; ++c) {
-    float v[32];
-    tc5::tmem_ld32(taddr + c * 32, v);
-    tc5::wait_ld();
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      float a0 = v[e], a1 = v[e + 1];
-      if (kMasked) {
-        a0 = (c * 32 + e < nvis) ? a0 : -INFINITY;
-        a1 = (c * 32 + e + 1 < nvis) ? a1 : -INFINITY;
-      }
-      m[(e >> 1) & 3] = max3(m[(e >> 1) & 3], a0, a1);
-    }
-  }
-  return max3(m[0], m[1], fmaxf(m[2], m[3]));
+// 2^d for an integer-valued d <= 0: exact, 0 below the normal range (and for
+// d = -inf).
+__device__ __forceinline__ float pow2_int(float d) {
+  return d < -126.f ? 0.f : __int_as_float((127 + static_cast<int>(d)) << 23);
 }
 
-// P = 2^(s * scale_log2 - u) for the visible keys (0 elsewhere), rounded to
-// bf16 and written back as pairs (keys k, k+1 in column k/2) over the first
-// 64 columns of the same S buffer, each chunk after it has been read.
-// Returns the row's sum of P (before rounding).
+// Multiply the bf16 pairs in kWords columns at taddr by the power of two f
+// (exact unless a value drops below the normal range).
+template <int kWords>
+__device__ __forceinline__ void scale_p(uint32_t taddr, float f) {
+  tc5::wait_st();                              // this thread's P stores to these columns
+  float w[32];
+  if (kWords == 16) tc5::tmem_ld16(taddr, w);
+  else tc5::tmem_ld32(taddr, w);
+  tc5::wait_ld();
+  uint32_t p[kWords];
+#pragma unroll
+  for (int j = 0; j < kWords; ++j) {
+    const uint32_t u = __float_as_uint(w[j]);
+    p[j] = pack_bf16x2(bf16lo(u) * f, bf16hi(u) * f);
+  }
+  if (kWords == 16) tc5::tmem_st16(taddr, p);
+  else tc5::tmem_st32u(taddr, p);
+}
+
+// This thread's 64 keys of one key tile: S from scol (two 32-column chunks),
+// P pairs to pcol (16 columns per chunk).  kbase = the first key's index in the
+// tile; keys kbase + e >= nvis are masked.  Returns the sum of P (before
+// rounding) against the m_ref in force at the end.
 template <bool kMasked>
-__device__ __forceinline__ float tile_exp(uint32_t taddr, int nvis, float sl2, float u) {
-  const uint64_t scale2 = pack2(sl2, sl2), shift2 = pack2(-u, -u);
-  uint64_t acc[4];
+__device__ __forceinline__ float half_tile(uint32_t scol, uint32_t pcol, int kbase, int nvis,
+                                           float sl2, float& m_ref) {
+  float psum = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = pack2(0.f, 0.f);
-#pragma unroll
-  for (int c = 0; c < kN / 32; ++c) {
+  for (int c = 0; c < 2; ++c) {
     float v[32];
-    tc5::tmem_ld32(taddr + c * 32, v);
+    tc5::tmem_ld32(scol + c * 32, v);
     tc5::wait_ld();
+    if (kMasked) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = (kbase + c * 32 + e < nvis) ? v[e] : -INFINITY;
+    }
+    float m4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m4[j] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) m4[(e >> 1) & 3] = max3(m4[(e >> 1) & 3], v[e], v[e + 1]);
+    const float mt = max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
+    const bool grow = mt > m_ref + kRescaleLog2;
+    if (__any_sync(0xffffffffu, grow)) {
+      const float m_new = grow ? ceilf(mt) : m_ref;
+      const float f = grow ? pow2_int(m_ref - m_new) : 1.f;
+      if (c == 1) scale_p<16>(pcol, f);
+      psum *= f;
+      m_ref = m_new;
+    }
+    const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
+    const uint64_t scale2 = pack2(sl2, sl2), shift2 = pack2(-u, -u);
+    uint64_t acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = pack2(0.f, 0.f);
     uint32_t pk[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-      const int k = c * 32 + 2 * q;
       float x0, x1;
       unpack2(fma2(pack2(v[2 * q], v[2 * q + 1]), scale2, shift2), x0, x1);
-      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-      if (kMasked) {
-        p0 = (k < nvis) ? p0 : 0.f;
-        p1 = (k + 1 < nvis) ? p1 : 0.f;
-      }
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);   // masked: 2^-inf = 0
       acc[q & 3] = add2(acc[q & 3], pack2(p0, p1));
       pk[q] = pack_bf16x2(p0, p1);
     }
-    tc5::tmem_st16(taddr + c * 16, pk);
+    tc5::tmem_st16(pcol + c * 16, pk);
+    const uint64_t t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+    float t0, t1;
+    unpack2(t, t0, t1);
+    psum += t0 + t1;
   }
-  const uint64_t t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-  float t0, t1;
-  unpack2(t, t0, t1);
-  return t0 + t1;
+  return psum;
 }
 
-// The output rows of tile x: O / l (bf16, or the fp32 partial of the split)
-// and the log-sum-exp.  Kept out of line: the indices are recomputed here
-// instead of living in registers through the softmax loop.
+// Swap one value per row with the other half of the warp pair: publish v in
+// this half's slot of the current parity, arrive on the pair's barrier, wait
+// (bounded) for the partner's arrival, read its slot.  Slots alternate by
+// parity, so a slot is rewritten only after the partner's next arrival, which
+// follows its read.
+__device__ __forceinline__ float pair_swap(float v, float* slots, uint64_t* bar, uint32_t& uses,
+                                           int half, int r, bool& ok) {
+  const int p = uses & 1;
+  slots[(p * 2 + half) * kM + r] = v;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  ok = warp_wait(bar, p) && ok;
+  ++uses;
+  return slots[(p * 2 + (half ^ 1)) * kM + r];
+}
+
+// This thread's half of an output row of tile x: O / l for dims 64h..64h+63
+// (bf16, or the fp32 partial of the split), and the log-sum-exp (half 0).
+// Kept out of line: the indices are recomputed here instead of living in
+// registers through the softmax loop.
 __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
-                                        int x, float m_ref, float l) {
-  const int r = threadIdx.x - x * kM;
+                                        int x, int half, float m_ref, float l) {
+  const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
   const int rg = w.mt * 2 * kM + x * kM + r;
   const int t0 = rg / a.group;
   // rows outside the sequence, or (inconsistent offsets) outside q/out: no write;
@@ -398,17 +452,18 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
   const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
   const int t = valid ? t0 : 0;
   const int hh = valid ? rg - t * a.group : 0;
-  const uint32_t o_cols =
-      tmem + (static_cast<uint32_t>((r >> 5) * 32) << 16) + kColO + x * kN;
+  const uint32_t o_cols = tmem + (static_cast<uint32_t>((r >> 5) * 32) << 16) + kColO +
+                          x * kN + half * (kHeadDim / 2);
   const int h = w.g * a.group + hh;
   const long long row = (w.q0 + t) * a.num_q_heads + h;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   const bool have_o = w.ntiles > 0;            // uniform over the CTA
+  const int d0 = half * (kHeadDim / 2);
   if (a.num_splits == 1) {
-    __nv_bfloat16* orow = a.out + row * kHeadDim;
+    __nv_bfloat16* orow = a.out + row * kHeadDim + d0;
 #pragma unroll 1
-    for (int c = 0; c < kHeadDim / 32; ++c) {
+    for (int c = 0; c < kHeadDim / 64; ++c) {
       float o[32];
       if (have_o) {
         tc5::tmem_ld32(o_cols + c * 32, o);
@@ -427,12 +482,12 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
         }
       }
     }
-    if (valid && a.lse_out != nullptr) a.lse_out[row] = lse;
+    if (valid && half == 0 && a.lse_out != nullptr) a.lse_out[row] = lse;
   } else {
     const long long prow = row * a.num_splits + w.j;
-    float* po = a.ws_o + prow * kHeadDim;
+    float* po = a.ws_o + prow * kHeadDim + d0;
 #pragma unroll 1
-    for (int c = 0; c < kHeadDim / 32; ++c) {
+    for (int c = 0; c < kHeadDim / 64; ++c) {
       float o[32];
       if (have_o) {
         tc5::tmem_ld32(o_cols + c * 32, o);
@@ -448,26 +503,29 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
         }
       }
     }
-    if (valid) a.ws_lse[prow] = lse;
+    if (valid && half == 0) a.ws_lse[prow] = lse;
   }
 }
 
 __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
-                             uint32_t tmem, int x) {
-  const int r = threadIdx.x - x * kM;          // row of tile x = tensor-memory lane
-  const int wq = r >> 5, lane = r & 31;
+                             float* xslots, uint32_t tmem, int x, int half) {
+  const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int r = wq * 32 + lane;                // row of tile x = tensor-memory lane
   const int rg = w.mt * 2 * kM + x * kM + r;
   const bool valid = rg < w.rows;
   const int t = valid ? rg / a.group : 0;
   // keys [k0, lim) are visible to this row
   const int lim = valid ? max(w.k0, min(w.k1, w.L - w.q_len + t + 1)) : w.k0;
   const uint32_t lanes = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const uint32_t s_cols = lanes + kColS + x * kN;
-  const uint32_t o_cols = lanes + kColO + x * kN;
+  const uint32_t s_cols = lanes + kColS + x * kN + half * (kN / 2);
+  const uint32_t o_cols = lanes + kColO + x * kN + half * (kHeadDim / 2);
   const float sl2 = a.scale_log2;
+  float* slots = xslots + x * 4 * kM;          // [parity][half][row] of tile x
+  uint64_t* xbar = &bars->xch[x][wq];
+  uint32_t uses = 0;
 
-  float m_ref = -INFINITY;                     // reference max (log2 units) of P
-  float l = 0.f;                               // sum of P
+  float m_ref = -INFINITY;                     // reference max (log2 units), integer once set
+  float l = 0.f;                               // this half's sum of P
   bool ok = true;
   for (int i = 0; i < w.ntiles; ++i) {
     // S_x(i) landed, and with it PV_x(i - 1): O_x is complete up to tile i - 1
@@ -480,15 +538,23 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
     // interior tiles (every row of the warp sees all 128 keys) skip the masks
     const bool whole = __all_sync(0xffffffffu, nvis == kN);
-    const float mx = whole ? tile_max<false>(s_cols, nvis) : tile_max<true>(s_cols, nvis);
-    const float m_tile = mx * sl2;
-    const bool grow = m_tile > m_ref + kRescaleLog2;
-    const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
-    if (grow) m_ref = m_tile;
-    const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
-    if (i > 0 && __any_sync(0xffffffffu, grow)) {
+    const float m_start = m_ref;
+    float psum = whole ? half_tile<false>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref)
+                       : half_tile<true>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref);
+    // one reference per row: the higher of the two halves'
+    const float m_row = fmaxf(m_ref, pair_swap(m_ref, slots, xbar, uses, half, r, ok));
+    if (!ok) break;
+    if (__any_sync(0xffffffffu, m_ref < m_row)) {
+      const float f = m_ref < m_row ? pow2_int(m_ref - m_row) : 1.f;
+      scale_p<32>(s_cols, f);
+      psum *= f;
+    }
+    m_ref = m_row;
+    const bool rose = m_row > m_start;         // -inf -> finite counts
+    const float alpha = rose ? pow2_int(m_start - m_row) : 1.f;
+    if (i > 0 && __any_sync(0xffffffffu, rose)) {
 #pragma unroll 1
-      for (int c = 0; c < kHeadDim / 32; ++c) {
+      for (int c = 0; c < kHeadDim / 64; ++c) {
         float o[32];
         tc5::tmem_ld32(o_cols + c * 32, o);
         tc5::wait_ld();
@@ -497,12 +563,11 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
         tc5::tmem_st32(o_cols + c * 32, o);
       }
     }
-    const float psum = whole ? tile_exp<false>(s_cols, nvis, sl2, u)
-                             : tile_exp<true>(s_cols, nvis, sl2, u);
     l = l * alpha + psum;
     // Tail tile: cache slots past the last visible key may hold anything
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
-    // their V rows are zeroed (by tile A, before either PV reads them).
+    // their V rows are zeroed (by tile A, each half its dims, before either
+    // PV reads them).
     if (x == 0 && kb + kN > w.key_end) {
       const int s = i & 1;
       if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
@@ -510,13 +575,10 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
         break;
       }
       if (kb + r >= w.key_end) {
-        uint8_t* vrow = smem + kOffV + s * kTile + r * 128;
+        uint8_t* vrow = smem + kOffV + s * kTile + half * kHalf + r * 128;
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          *reinterpret_cast<uint4*>(vrow + c * 16) = z;
-          *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
-        }
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = z;
       }
       tc5::fence_smem_for_async();
     }
@@ -529,19 +591,21 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     ok = warp_wait(&bars->pv_done[x], 0);
     tc5::fence_after_sync();
   }
+  // the row's sum of P: both halves'
+  if (ok) l += pair_swap(l, slots, xbar, uses, half, r, ok);
   if (!ok) {
     bars->abort = 1;
     report(a.status_flags, kFlagTimeout);
     return;
   }
-  write_rows(a, w, tmem, x, m_ref, l);
+  write_rows(a, w, tmem, x, half, m_ref, l);
 }
 
 // ------------------------------------------------------------------ kernel
 
-// 10 warps: two of the SM's four sub-partitions hold three of them, so a
-// thread gets at most 168 registers (16,384 per sub-partition).
-__global__ void __launch_bounds__(kThreads, 1)
+// 18 warps: two of the SM's four sub-partitions hold five of them, so a
+// thread gets at most 96 registers (16,384 per sub-partition).
+__global__ void __maxnreg__(96)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -569,7 +633,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->p_full[x], 4);
+      mbar_init(&bars->p_full[x], kSoftmaxWarps / 2);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->xch[x][q], 2);
       mbar_init(&bars->pv_done[x], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -579,11 +644,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
 
-  if (warp < 8) {
-    // Q tiles: thread i loads row i % 128 of tile i / 128 (row = (token, q head
-    // of the group)), two swizzled 64-dim halves
-    const int x = threadIdx.x / kM, r = threadIdx.x % kM;
-    const int rg = w.mt * 2 * kM + threadIdx.x;
+  if (warp < kSoftmaxWarps) {
+    // Q tiles: thread i loads 64 dims (half i / 256) of row i % 128 of tile
+    // (i / 128) % 2 (row = (token, q head of the group)), one swizzled half
+    const int row = threadIdx.x % (2 * kM), dh = threadIdx.x / (2 * kM);
+    const int x = row / kM, r = row % kM;
+    const int rg = w.mt * 2 * kM + row;
     const int t0 = rg / a.group;
     const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
     const int t = valid ? t0 : 0;
@@ -593,9 +659,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
         static_cast<long long>(w.g * a.group + hh) * a.q_stride_h);
     uint8_t* qt = smem + kOffQ + x * kTile;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(qt + (c >> 3) * kHalf + swz128(r, c & 7)) = v;
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = valid ? __ldg(src + dh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(qt + dh * kHalf + swz128(r, c)) = v;
     }
     tc5::fence_smem_for_async();
   }
@@ -605,10 +671,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   pdl_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp < 4) {
-    softmax_rows(a, w, smem, bars, tmem, 0);
-  } else if (warp < 8) {
-    if (w.has_b) softmax_rows(a, w, smem, bars, tmem, 1);
+  if (warp < kSoftmaxWarps) {
+    // warp = 8 x + 4 half + lane quadrant
+    const int x = warp >> 3, half = (warp >> 2) & 1;
+    if (x == 0 || w.has_b)
+      softmax_rows(a, w, smem, bars, reinterpret_cast<float*>(smem + kOffSlots), tmem, x, half);
   } else if (warp == kProducerWarp) {
     int n = 0;
     produce(a, w, &kmap, &vmap, smem, bars, &n);
