@@ -263,17 +263,26 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
   const int n = w.ntiles;
   constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(kM, kN, false);
   constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kM, kHeadDim, true);
+  // Descriptors as 32-bit halves; every operand of this kernel shares the high
+  // half (stride offset 1024, version, 128-byte swizzle), and a 16-element
+  // step moves only the low half's start address.
+  const uint64_t d0 = desc_k_major(smem_addr(smem + kOffQ), 0);
+  const uint32_t hi = static_cast<uint32_t>(d0 >> 32);
+  const uint32_t q_lo = static_cast<uint32_t>(d0);
+  const uint32_t k_lo = static_cast<uint32_t>(desc_k_major(smem_addr(smem + kOffK), 0));
+  const uint32_t v_lo = static_cast<uint32_t>(desc_v(smem_addr(smem + kOffV), 0));
   // S_x(i) = Q_x K_i^T
   auto mma_s = [&](int x, int i) -> bool {
     const int s = i & 1;
     if (x == 0 && !mbar_wait(&bars->full_k[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
-    const uint32_t q = smem_addr(smem + kOffQ + x * kTile);
-    const uint32_t kt = smem_addr(smem + kOffK + s * kTile);
+    const uint32_t qa = q_lo + (x * kTile >> 4), kb = k_lo + (s * kTile >> 4);
+    const uint32_t dst = tmem + kColS + x * kN;
 #pragma unroll
-    for (int kk = 0; kk < kHeadDim / 16; ++kk)
-      tc5::mma_f16(tmem + kColS + x * kN, desc_k_major(q, kk), desc_k_major(kt, kk), idesc_s,
-                   kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+      const uint32_t step = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+      tc5::mma_f16_lh(dst, qa + step, hi, kb + step, hi, idesc_s, kk > 0 ? 1u : 0u);
+    }
     tc5::commit(&bars->s_full[x]);
     if (x == last) tc5::commit(&bars->empty_k[s]);
     return true;
@@ -284,13 +293,13 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     if (!mbar_wait(&bars->p_full[x], i & 1)) return false;
     if (x == 0 && !mbar_wait(&bars->full_v[s], (i >> 1) & 1)) return false;
     tc5::fence_after_sync();
-    const uint32_t vt = smem_addr(smem + kOffV + s * kTile);
+    const uint32_t vb = v_lo + (s * kTile >> 4);
+    const uint32_t dst = tmem + kColO + x * kN, p0 = tmem + kColS + x * kN;
     // P_x: 16 keys per step = 8 columns of bf16 pairs; keys 64h.. at column 64h
 #pragma unroll
     for (int ks = 0; ks < kN / 16; ++ks)
-      tc5::mma_f16_ts(tmem + kColO + x * kN,
-                      tmem + kColS + x * kN + (ks >> 2) * (kN / 2) + (ks & 3) * 8,
-                      desc_v(vt, ks), idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+      tc5::mma_f16_ts_lh(dst, p0 + (ks >> 2) * (kN / 2) + (ks & 3) * 8, vb + (ks * 2048 >> 4),
+                         hi, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
     if (i == n - 1) tc5::commit(&bars->pv_done[x]);
     if (x == last) tc5::commit(&bars->empty_v[s]);
     return true;
