@@ -90,6 +90,11 @@ PREFILL_WORKLOADS = {
     "prefill_gqa8_8x512": ("chunked_prefill", {"Hq": 32, "Hkv": 4},
                            "chunked prefill 32q/4kv D128 bs16, batch 8 x 512-token chunk, "
                            "prior context U[0, 6144]"),
+    "prefill_19x512_ctx16k": ("chunked_prefill",
+                              {"batch": 19, "chunk": 512, "lo": 16384, "hi": 16384},
+                              "chunked prefill 16q/8kv D128 bs16, batch 19 x 512-token chunk "
+                              "after 16384 prior tokens (a long prompt's late chunks; 608 CTAs "
+                              "= 4 waves on 152 SMs)"),
     "prefill_varlen_16": ("varlen_prefill", {},
                           "varlen prefill 16q/8kv D128 bs16, 16 fresh prompts of U[128, 2048] "
                           "tokens, packed"),
@@ -113,6 +118,10 @@ SWEEP = ([(f"decode_{b}x{c}", -1, "batch x context") for b in (1, 8, 32, 64)
             ("verify_32x5", -1, "speculative verify"),
             ("decode_gqa8_64x4096", -1, "GQA-8 uniform"),
             ("decode_gqa4_32x8192", -1, "GQA-4 uniform")])
+
+# The prefill configurations timed after the decode study in the default run.
+PREFILL_SWEEP = ("prefill_4x2048", "prefill_8x512", "prefill_gqa8_8x512", "prefill_varlen_16",
+                 "prefill_19x512_ctx16k")
 
 # The oracle's CPU timing covers these decode configurations.
 CPU_BASELINE_WORKLOADS = ("decode_64x8192", "decode_long_8x32768", "decode_gqa8_64",
@@ -829,6 +838,31 @@ def sweep_point(runner, steps, warmup, peak, group):
     }
 
 
+def prefill_point(runner, steps, warmup, tpeak):
+    """One prefill configuration of the default run: the step (append +
+    prefill call) and the prefill call timed as a prefill headline is."""
+    p = runner.p
+    t0 = time.time()
+    runner.warm(warmup)
+    total_ms = runner.time_value(steps)
+    app, dec = runner.time_calls(steps)
+    t1 = time.time()
+    ms = total_ms / steps
+    dec_ms = statistics.fmean(dec)
+    flops = attention_flops(p)
+    tflops = flops / (dec_ms * 1e-3) / 1e12
+    return {
+        "workload": runner.name, "batch": p.B, "new_tokens": p.T, "ctx_max": p.max_seq_len,
+        "heads_q": p.Hq, "heads_kv": p.Hkv, "num_splits": runner.S, "steps": steps,
+        "ms_per_step": round(ms, 5), "step_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "append_ms": round(statistics.fmean(app), 5),
+        "prefill_ms": round(dec_ms, 5), "tflops": round(tflops, 2),
+        "frac": round(tflops / tpeak, 4), "algorithmic_flops_per_launch": flops,
+        "l2": "inputs > 4x L2" if runner.big_inputs else "cold clean L2 before every step",
+        "window": (t0, t1),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1007,6 +1041,20 @@ def main():
             del r
         cache.clear()
         torch.cuda.empty_cache()
+    # the prefill configurations (tensor-core kernel), N = 1 only, same timing
+    psweep = None
+    if world == 1 and not args.no_sweep and not prefill:
+        only = {s for s in args.sweep_only.split(",") if s}
+        tpeak, _ = load_peaks("bf16_tflops", 1900.0)
+        psweep = []
+        for name in PREFILL_SWEEP:
+            if only and name not in only:
+                continue
+            torch.cuda.empty_cache()
+            r = StepRunner(lib, name, build_problem(name, dev), -1, dev, stream, flush)
+            psweep.append(prefill_point(r, args.sweep_steps, 5, tpeak))
+            del r
+        torch.cuda.empty_cache()
     clocks.stop()
     line["clocks"] = clocks.window(t_head0, t_head1)
     if sweep is not None:
@@ -1020,6 +1068,16 @@ def main():
                               "from a second pass with events around each call; frac = decode "
                               "GB/s / measured HBM copy GB/s; traffic = 1-pass ncu DRAM bytes "
                               "of one decode launch where captured on the current sources")
+    if psweep is not None:
+        for rec in psweep:
+            clk = clocks.window(*rec.pop("window"))
+            rec["sm_mhz"] = clk["sm_mhz"] if clk else None
+            rec["clock_reasons"] = clk["reasons"] if clk else None
+        line["prefill_sweep"] = psweep
+        line["prefill_sweep_note"] = ("chunked and varlen prefill on the tcgen05 kernel: step = "
+                                      "append + prefill call; prefill_ms from a second pass "
+                                      "with events around each call; frac = TFLOP/s / measured "
+                                      "bf16 cuBLAS burst peak")
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not prefill:
         cb = run_cpu_baseline_child(args.cpu_seconds)

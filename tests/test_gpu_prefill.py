@@ -324,6 +324,16 @@ def test_prefill_4x2048_workload_sampled(lib):
                     np.random.default_rng(45))
 
 
+def test_prefill_19x512_ctx16k_workload_sampled(lib):
+    """The long-context chunk workload (19 x 512-token chunks after 16384
+    prior tokens, four full waves of CTAs) in the benchmark's configuration."""
+    p = workloads.chunked_prefill(device="cuda", batch=19, chunk=512, lo=16384, hi=16384)
+    S = lib.choose_prefill_splits(p.B, p.Hkv, p.q_len, p.Hq // p.Hkv, p.max_seq_len)
+    out, lse = _prefill(lib, p, num_splits=S)
+    _sampled_tokens(lib, p, out.reshape(p.T, p.Hq, p.D), lse.reshape(p.T, p.Hq),
+                    np.random.default_rng(47), per_seq=1)
+
+
 def test_varlen_prefill_16_workload_sampled(lib):
     """The varlen benchmark workload: 16 fresh prompts of U[128, 2048] tokens."""
     p = workloads.varlen_prefill(device="cuda")
