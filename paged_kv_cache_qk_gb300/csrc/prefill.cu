@@ -28,13 +28,18 @@
 //              reference max with the other half once per tile, rescales its
 //              half of O in tensor memory only when the max grew by more than
 //              2^8 (P <= 2^8 otherwise), and writes its 64 output dims;
-//   warp 16    TMA producer: one box per (page, 64-dim half) of K and of V;
+//   warp 16    TMA producer: the Q tiles at set-up (one box per row tile and
+//              64-dim half, where q's layout allows), then one box per (page,
+//              64-dim half) of K and of V;
 //   warp 17    allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
 //              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
 //                               operands in shared memory),
 //              O_x += P_x V_i   (M 128 rows, N 128 dims, K 128 keys; P from
 //                               tensor memory, V from shared memory).
+// Output: a whole row tile (inside its sequence, single split) is staged as
+// bf16 in its Q tile's shared memory and leaves as two TMA boxes; partial
+// tiles and split partials are stored by the softmax threads.
 // S_x(i+1) overwrites the columns that held P_x(i): the MMAs of one thread
 // run in issue order, and PV_x(i) is issued first.  The commit that signals
 // S_x(i+1) also covers PV_x(i), so softmax x may rescale O_x as soon as it
@@ -55,6 +60,11 @@
 #include "device_common.cuh"
 #include "prefill.h"
 #include "tc5.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
 
 namespace pkvqk {
 
@@ -88,6 +98,8 @@ struct Bars {
   uint64_t pv_done[2];                           // the last O_x += P_x V finished
   uint64_t drain;                                // MMA thread's own completion (timeout path)
   uint64_t xch[2][4];                            // warp pair (tile, lane quadrant) swaps
+  uint64_t q_full;                               // Q tiles landed (TMA)
+  uint64_t o_staged[2];                          // tile x's output rows staged for TMA
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -125,6 +137,31 @@ __device__ __forceinline__ void tma_load_5d_keep(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
       "r"(smem_addr(bar))
       : "memory");
+}
+
+// One box of a row-tile map (q): 64 dims x group heads x 128 / group tokens.
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// The same box from shared memory to out, then wait until shared memory has
+// been read (the CTA may leave after that).
+__device__ __forceinline__ void tma_store_rows(const void* src, const CUtensorMap* map, int c0,
+                                               int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(src))
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -305,7 +342,9 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     return true;
   };
   bool ok = true;
-  if (n > 0) {
+  // Q tiles by TMA (issued at set-up)
+  if (a.q_tma && n > 0) ok = mbar_wait(&bars->q_full, 0);
+  if (ok && n > 0) {
     ok = mma_s(0, 0);
     if (ok && w.has_b) ok = mma_s(1, 0);
   }
@@ -452,6 +491,7 @@ __device__ __forceinline__ float pair_swap(float v, float* slots, uint64_t* bar,
 // Kept out of line: the indices are recomputed here instead of living in
 // registers through the softmax loop.
 __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
+                                        uint8_t* smem, Bars* bars, const CUtensorMap* omap,
                                         int x, int half, float m_ref, float l) {
   const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
   const int rg = w.mt * 2 * kM + x * kM + r;
@@ -469,6 +509,51 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
   const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   const bool have_o = w.ntiles > 0;            // uniform over the CTA
   const int d0 = half * (kHeadDim / 2);
+  // a whole row tile inside the sequence and inside out (uniform over the
+  // tile): staged in Q_x's shared memory (no MMA reads it any more), then one
+  // TMA store per 64-dim half
+  const int row0 = w.mt * 2 * kM + x * kM;
+  const long long tok0 = w.q0 + row0 / a.group;
+  const bool whole_tile = a.o_tma && a.num_splits == 1 && row0 + kM <= w.rows && tok0 >= 0 &&
+                          w.q0 + (row0 + kM - 1) / a.group < a.total_q;
+  if (whole_tile) {
+    uint8_t* stage = smem + kOffQ + x * kTile + half * kHalf;
+#pragma unroll 1
+    for (int c = 0; c < kHeadDim / 64; ++c) {
+      float o[32];
+      if (have_o) {
+        tc5::tmem_ld32(o_cols + c * 32, o);
+        tc5::wait_ld();
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint4 pk;
+        const float* y = o + q8 * 8;
+        pk.x = have_o ? pack_bf16x2(y[0] * inv, y[1] * inv) : 0u;
+        pk.y = have_o ? pack_bf16x2(y[2] * inv, y[3] * inv) : 0u;
+        pk.z = have_o ? pack_bf16x2(y[4] * inv, y[5] * inv) : 0u;
+        pk.w = have_o ? pack_bf16x2(y[6] * inv, y[7] * inv) : 0u;
+        *reinterpret_cast<uint4*>(stage + swz128(r, c * 4 + q8)) = pk;
+      }
+    }
+    tc5::fence_smem_for_async();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bars->o_staged[x]);
+    if (half == 0 && a.lse_out != nullptr) a.lse_out[row] = lse;
+    if (threadIdx.x == x * 2 * kM) {           // warp 8x, lane 0
+      if (mbar_wait(&bars->o_staged[x], 0)) {
+        const uint8_t* src = smem + kOffQ + x * kTile;
+        const int hc = w.g * a.group, tc = static_cast<int>(tok0);
+        tma_store_rows(src, omap, 0, hc, tc);
+        tma_store_rows(src + kHalf, omap, 64, hc, tc);
+        tma_store_commit_and_wait_read();
+      } else {
+        bars->abort = 1;
+        report(a.status_flags, kFlagTimeout);
+      }
+    }
+    return;
+  }
   if (a.num_splits == 1) {
     __nv_bfloat16* orow = a.out + row * kHeadDim + d0;
 #pragma unroll 1
@@ -517,7 +602,8 @@ __device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uin
 }
 
 __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem, Bars* bars,
-                             float* xslots, uint32_t tmem, int x, int half) {
+                             const CUtensorMap* omap, float* xslots, uint32_t tmem, int x,
+                             int half) {
   const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int r = wq * 32 + lane;                // row of tile x = tensor-memory lane
   const int rg = w.mt * 2 * kM + x * kM + r;
@@ -607,7 +693,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     report(a.status_flags, kFlagTimeout);
     return;
   }
-  write_rows(a, w, tmem, x, half, m_ref, l);
+  write_rows(a, w, tmem, smem, bars, omap, x, half, m_ref, l);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -616,7 +702,9 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
 // thread gets at most 96 registers (16,384 per sub-partition).
 __global__ void __maxnreg__(96)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = reinterpret_cast<Bars*>(smem + kDataBytes);
@@ -645,15 +733,30 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(&bars->p_full[x], kSoftmaxWarps / 2);
       for (int q = 0; q < 4; ++q) mbar_init(&bars->xch[x][q], 2);
       mbar_init(&bars->pv_done[x], 1);
+      mbar_init(&bars->o_staged[x], kSoftmaxWarps / 2);
     }
+    mbar_init(&bars->q_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     issued = 0;
     fence_barrier_init();
+    // Q tiles by TMA: one box per (row tile, 64-dim half), rows past q or
+    // before it read as zeros, rows of a following sequence are masked
+    if (a.q_tma && w.ntiles > 0) {
+      prefetch_tensormap(&qmap);
+      const int nt = w.has_b ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, nt * kTile);
+      for (int x = 0; x < nt; ++x) {
+        const int tok = static_cast<int>(w.q0 + (w.mt * 2 * kM + x * kM) / a.group);
+        for (int dh = 0; dh < 2; ++dh)
+          tma_load_rows(smem + kOffQ + x * kTile + dh * kHalf, &qmap, &bars->q_full, dh * 64,
+                        w.g * a.group, tok);
+      }
+    }
   }
   if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
 
-  if (warp < kSoftmaxWarps) {
+  if (warp < kSoftmaxWarps && !a.q_tma) {
     // Q tiles: thread i loads 64 dims (half i / 256) of row i % 128 of tile
     // (i / 128) % 2 (row = (token, q head of the group)), one swizzled half
     const int row = threadIdx.x % (2 * kM), dh = threadIdx.x / (2 * kM);
@@ -684,11 +787,17 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     // warp = 8 x + 4 half + lane quadrant
     const int x = warp >> 3, half = (warp >> 2) & 1;
     if (x == 0 || w.has_b)
-      softmax_rows(a, w, smem, bars, reinterpret_cast<float*>(smem + kOffSlots), tmem, x, half);
+      softmax_rows(a, w, smem, bars, &omap, reinterpret_cast<float*>(smem + kOffSlots), tmem, x,
+                   half);
   } else if (warp == kProducerWarp) {
     int n = 0;
     produce(a, w, &kmap, &vmap, smem, bars, &n);
-    if (threadIdx.x == kProducerWarp * 32) issued = n;
+    if (threadIdx.x == kProducerWarp * 32) {
+      issued = n;
+      // the Q copies have landed before the CTA can leave (done long ago
+      // unless the MMA thread gave up)
+      if (a.q_tma && w.ntiles > 0) mbar_wait(&bars->q_full, 0);
+    }
   } else {
     if ((threadIdx.x & 31) == 0) issue_mmas(a, w, smem, bars, tmem);
     __syncwarp();
@@ -702,18 +811,70 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point, looked up
+// once; nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 row_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D view (128 dims, heads, tokens) of q or out, strides in bytes, with a box
+// of (64 dims, group heads, 128 / group tokens) and 128-byte swizzle: one box
+// is one 64-dim half of a 128-row tile in the packed row order
+// r = t * group + h % group, laid out as the MMA operand (and the output
+// staging) expects.  False where the layout does not allow such a box (group
+// not a power of two up to 128, base or strides not multiples of 16 bytes).
+bool encode_rows_map(CUtensorMap* map, const void* base, long long tokens, int heads,
+                     long long stride_h, long long stride_t, int group) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = row_map_encoder();
+  if (encode == nullptr || base == nullptr || tokens < 1 || group < 1 || group > 128 ||
+      (group & (group - 1)) != 0 || heads < group)
+    return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || stride_h % 16 != 0 || stride_t % 16 != 0 ||
+      stride_h <= 0 || stride_t <= 0)
+    return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride_h), static_cast<cuuint64_t>(stride_t)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kM / group)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const PrefillArgs& a, cudaStream_t stream) {
+                                 const PrefillArgs& args, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t e = set_smem_limit_once(paged_prefill_kernel, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
+  PrefillArgs a = args;
+  CUtensorMap qmap, omap;
+  std::memset(&qmap, 0, sizeof(qmap));
+  std::memset(&omap, 0, sizeof(omap));
+  a.q_tma = encode_rows_map(&qmap, a.q, a.total_q, a.num_q_heads, a.q_stride_h * 2,
+                            a.q_stride_t * 2, a.group) ? 1 : 0;
+  a.o_tma = (a.num_splits == 1 &&
+             encode_rows_map(&omap, a.out, a.total_q, a.num_q_heads, kHeadDim * 2,
+                             static_cast<long long>(a.num_q_heads) * kHeadDim * 2, a.group))
+                ? 1 : 0;
   const long long gx = static_cast<long long>(a.m_tiles) * a.num_kv_heads * a.num_splits;
   return launch_pdl(paged_prefill_kernel, dim3(static_cast<unsigned>(gx), a.batch),
-                    dim3(kThreads), kSmemBytes, stream, kmap, vmap, a);
+                    dim3(kThreads), kSmemBytes, stream, kmap, vmap, qmap, omap, a);
 }
 
 }  // namespace pkvqk

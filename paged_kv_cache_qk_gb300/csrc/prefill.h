@@ -35,6 +35,9 @@ struct PrefillArgs {
   float* ws_o;                     // num_splits > 1: [rows, S, 128] normalised partials
   float* ws_lse;                   // num_splits > 1: [rows, S]
   int32_t* status_flags;
+  // set by launch_paged_prefill: q rows arrive by TMA through qmap, and whole
+  // row tiles of out (num_splits == 1) leave by TMA through omap
+  int32_t q_tma, o_tma;
 };
 
 // Shared-memory bytes one CTA of the kernel takes (one CTA per SM).
@@ -42,6 +45,7 @@ int prefill_smem_bytes();
 
 // Tensor maps: 5-D cache views with a box of (64 dims, b slots, 1 half, 1 head,
 // 1 block), b = the largest power of two dividing block_size, at most 128.
+// The q and out row-tile maps are built here (where the layouts allow them).
 cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillArgs& a, cudaStream_t stream);
 

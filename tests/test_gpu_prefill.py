@@ -52,7 +52,7 @@ def _check_all(p, out, lse, what, scale=None):
 
 # (Hq, Hkv, q_len, block_size, priors): row tiles of 128 packed (token, head)
 # rows -- exact, ragged, several per kv head; fresh prompts (prior 0), short
-# and long priors; GQA groups 1, 2, 8; page sizes 16 .. 256 and a
+# and long priors; GQA groups 1, 2, 3, 8; page sizes 16 .. 256 and a
 # non-power-of-two 48
 CASES = [
     (16, 8, 64, 16, [0, 100, 300]),
@@ -70,6 +70,10 @@ CASES = [
     (16, 8, 290, 48, [61, 190]),
     (32, 4, 100, 32, [250, 1]),
     (16, 16, 700, 64, [0, 700]),
+    # a group of 3: tiles start mid-token, so Q comes in and the output rows go
+    # out by thread loads and stores instead of the row-tile TMA boxes
+    (12, 4, 90, 16, [100, 0]),
+    (12, 4, 200, 32, [0, 333]),
 ]
 
 
