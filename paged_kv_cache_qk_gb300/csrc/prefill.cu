@@ -488,9 +488,11 @@ __device__ __forceinline__ float pair_swap(float v, float* slots, uint64_t* bar,
 
 // This thread's half of an output row of tile x: O / l for dims 64h..64h+63
 // (bf16, or the fp32 partial of the split), and the log-sum-exp (half 0).
-// Kept out of line: the indices are recomputed here instead of living in
-// registers through the softmax loop.
-__device__ __noinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
+// Inline: out of line, its code was cold in the SM's instruction cache at
+// every CTA's end (1.2 us from the last swap to the first output load,
+// against 0.5 inline), which cost more than the few spills inlining brings
+// at 96 registers.
+__device__ __forceinline__ void write_rows(const PrefillArgs& a, const Work& w, uint32_t tmem,
                                         uint8_t* smem, Bars* bars, const CUtensorMap* omap,
                                         int x, int half, float m_ref, float l) {
   const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
@@ -682,6 +684,8 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->p_full[x]);
   }
+  // write_rows reads the work item from the stack, where the long loop has
+  // let it fall out of L1 (~1 us back from L2): fetch it during the last PV
   if (ok && w.ntiles > 0) {
     ok = warp_wait(&bars->pv_done[x], 0);
     tc5::fence_after_sync();
@@ -704,7 +708,8 @@ __global__ void __maxnreg__(96)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap,
-                     const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
+                     const __grid_constant__ CUtensorMap omap,
+                     const __grid_constant__ PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Bars* bars = reinterpret_cast<Bars*>(smem + kDataBytes);
