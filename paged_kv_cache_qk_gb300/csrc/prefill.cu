@@ -183,12 +183,26 @@ struct Work {
 
 __device__ Work decode_work(const PrefillArgs& a) {
   Work w;
-  int x = blockIdx.x;
-  w.mt = x % a.m_tiles;
-  x /= a.m_tiles;
-  w.g = x % a.num_kv_heads;
-  w.j = x / a.num_kv_heads;
-  w.b = blockIdx.y;
+  if (a.mt_major) {
+    // the launch order runs over all sequences' last row tiles first: for
+    // fresh prompts a row tile's keys grow with its index, so this hands the
+    // longest work out first
+    const int per_mt = gridDim.y * a.num_kv_heads * a.num_splits;
+    int x = blockIdx.y * gridDim.x + blockIdx.x;
+    w.mt = a.m_tiles - 1 - x / per_mt;
+    x %= per_mt;
+    w.b = x / (a.num_kv_heads * a.num_splits);
+    x %= a.num_kv_heads * a.num_splits;
+    w.g = x / a.num_splits;
+    w.j = x % a.num_splits;
+  } else {
+    int x = blockIdx.x;
+    w.mt = x % a.m_tiles;
+    x /= a.m_tiles;
+    w.g = x % a.num_kv_heads;
+    w.j = x / a.num_kv_heads;
+    w.b = blockIdx.y;
+  }
   const long long cap = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
   const long long L = min(static_cast<long long>(max(a.seq_lens[w.b], 0)), cap);
   w.L = static_cast<int>(L);
@@ -880,6 +894,7 @@ cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vma
   CUtensorMap qmap, omap;
   std::memset(&qmap, 0, sizeof(qmap));
   std::memset(&omap, 0, sizeof(omap));
+  a.mt_major = a.cu_seqlens_q != nullptr ? 1 : 0;
   a.q_tma = encode_rows_map(&qmap, a.q, a.total_q, a.num_q_heads, a.q_stride_h * 2,
                             a.q_stride_t * 2, a.group) ? 1 : 0;
   a.o_tma = (a.num_splits == 1 &&

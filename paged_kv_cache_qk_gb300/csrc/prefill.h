@@ -38,6 +38,9 @@ struct PrefillArgs {
   // set by launch_paged_prefill: q rows arrive by TMA through qmap, and whole
   // row tiles of out (num_splits == 1) leave by TMA through omap
   int32_t q_tma, o_tma;
+  // set by launch_paged_prefill: the grid runs over (row tile descending,
+  // sequence, kv head, split) instead of (sequence, split, kv head, row tile)
+  int32_t mt_major;
 };
 
 // Shared-memory bytes one CTA of the kernel takes (one CTA per SM).
