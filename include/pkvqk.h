@@ -390,7 +390,7 @@ PKVQK_API size_t pkvqk_prefill_workspace_bytes(int32_t batch, int32_t q_len,
  *   max_seq_len_hint  host int >= the longest seq_len (0 = max_blocks_per_seq*block_size)
  *   workspace     device, >= pkvqk_prefill_workspace_bytes(...) (NULL if 0)
  * Supported: head_dim 128, Hq % Hkv == 0, 1 <= q_len <= 16384,
- * q_len*Hq/Hkv <= 65536.  One CTA per SM (192 KiB of shared memory and 512
+ * q_len*Hq/Hkv <= 65536.  One CTA per SM (197 KiB of shared memory and 512
  * tensor-memory columns each).
  */
 PKVQK_API pkvqk_status pkvqk_paged_prefill(
