@@ -196,8 +196,9 @@ __device__ Work decode_work(const PrefillArgs& a) {
     w.g = x / a.num_splits;
     w.j = x % a.num_splits;
   } else {
+    // within a (sequence, kv head) the last row tile (the most keys) first
     int x = blockIdx.x;
-    w.mt = x % a.m_tiles;
+    w.mt = a.m_tiles - 1 - x % a.m_tiles;
     x /= a.m_tiles;
     w.g = x % a.num_kv_heads;
     w.j = x / a.num_kv_heads;

@@ -39,7 +39,8 @@ struct PrefillArgs {
   // row tiles of out (num_splits == 1) leave by TMA through omap
   int32_t q_tma, o_tma;
   // set by launch_paged_prefill: the grid runs over (row tile descending,
-  // sequence, kv head, split) instead of (sequence, split, kv head, row tile)
+  // sequence, kv head, split) instead of (sequence, split, kv head, row tile
+  // descending)
   int32_t mt_major;
 };
 
