@@ -132,6 +132,20 @@ def test_prefill_equals_verify_decode_kernel(lib):
     assert (lse_p - lse_d).abs().max().item() <= 1e-3
 
 
+def test_prefill_without_lse_output(lib):
+    """lse_out = NULL: the outputs are the same bits as with it, through both
+    output paths (whole row tiles leave by TMA boxes, the ragged last tile by
+    thread stores; 300 tokens x group 2 = two whole tiles and a partial one)."""
+    p = _problem(16, 8, 300, 16, [37, 0, 513], seed=81)
+    out_l, lse = _prefill(lib, p)
+    out = torch.full_like(out_l, float("nan"))
+    lib.paged_prefill(p.q, p.k_cache, p.v_cache, p.block_tables, p.seq_lens, out, q_len=p.q_len,
+                      max_seq_len_hint=p.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_l)
+    assert torch.isfinite(lse).all()
+
+
 def test_prefill_rows_without_keys(lib):
     # seq_len below q_len (tokens whose position would be negative) and an
     # empty sequence: their rows see no key -> 0 output and lse = -inf
