@@ -52,7 +52,7 @@ def _check_all(p, out, lse, what, scale=None):
 
 # (Hq, Hkv, q_len, block_size, priors): row tiles of 128 packed (token, head)
 # rows -- exact, ragged, several per kv head; fresh prompts (prior 0), short
-# and long priors; GQA groups 1, 2, 3, 8; page sizes 16 .. 256 and a
+# and long priors; GQA groups 1, 2, 3, 4, 8, 16; page sizes 16 .. 256 and a
 # non-power-of-two 48
 CASES = [
     (16, 8, 64, 16, [0, 100, 300]),
@@ -74,6 +74,10 @@ CASES = [
     # out by thread loads and stores instead of the row-tile TMA boxes
     (12, 4, 90, 16, [100, 0]),
     (12, 4, 200, 32, [0, 333]),
+    # the TMA row-tile boxes for groups 4 and 16 (64 dims x G heads x 128/G
+    # tokens): whole and ragged tiles
+    (32, 8, 70, 32, [0, 200]),
+    (16, 1, 40, 16, [70, 3]),
 ]
 
 
