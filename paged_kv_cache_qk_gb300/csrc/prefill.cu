@@ -12,7 +12,9 @@
 // unless the caller gives one.  q_len is either one value for the batch or,
 // varlen (the FlashAttention-2 varlen role of Summary item 1), per sequence
 // from cumulative row offsets; the grid covers the longest, and row tiles past
-// a shorter sequence's rows do nothing.
+// a shorter sequence's rows do nothing.  Launch order: a (sequence, kv head)'s
+// row tiles last-first (the most keys first); varlen grids run every
+// sequence's last row tiles first.
 //
 // One CTA = two tiles A and B of 128 packed rows r = t * group + (h % group)
 // of one (sequence, kv head) -- 256 consecutive rows -- restricted to one
