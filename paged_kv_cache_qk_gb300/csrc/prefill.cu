@@ -110,6 +110,12 @@ constexpr int kOffSlots = kDataBytes + 256;   // pair-swap slots [tile][parity][
 constexpr int kSlotBytes = 2 * 2 * 2 * kM * 4;
 constexpr int kSmemBytes = kOffSlots + kSlotBytes + 1024;   // + alignment slack
 
+// x / group for x >= 0: a shift where the group is a power of two (the
+// usual case), else the division.
+__device__ __forceinline__ int div_group(const PrefillArgs& a, int x) {
+  return a.group_shift >= 0 ? (x >> a.group_shift) : x / a.group;
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_addr(p);
   return p + (((s + 1023u) & ~1023u) - s);
@@ -224,7 +230,7 @@ __device__ Work decode_work(const PrefillArgs& a) {
   const int row0 = w.mt * 2 * kM;
   w.has_b = row0 + kM < w.rows;
   const int last_row = min(row0 + 2 * kM - 1, w.rows - 1);
-  const int t_last = last_row / a.group;
+  const int t_last = div_group(a, max(last_row, 0));   // rows == 0: no tiles either way
   w.key_end = max(w.k0, min(w.k1, w.L - w.q_len + t_last + 1));
   w.ntiles = row0 < w.rows ? (w.key_end - w.k0 + kN - 1) / kN : 0;
   return w;
@@ -523,7 +529,7 @@ __device__ __forceinline__ void write_rows(const PrefillArgs& a, const Work& w, 
                                         int x, int half, float m_ref, float l) {
   const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
   const int rg = w.mt * 2 * kM + x * kM + r;
-  const int t0 = rg / a.group;
+  const int t0 = div_group(a, rg);
   // rows outside the sequence, or (inconsistent offsets) outside q/out: no write;
   // every lane still takes part in the warp-wide tensor-memory loads below
   const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
@@ -541,9 +547,9 @@ __device__ __forceinline__ void write_rows(const PrefillArgs& a, const Work& w, 
   // tile): staged in Q_x's shared memory (no MMA reads it any more), then one
   // TMA store per 64-dim half
   const int row0 = w.mt * 2 * kM + x * kM;
-  const long long tok0 = w.q0 + row0 / a.group;
+  const long long tok0 = w.q0 + div_group(a, row0);
   const bool whole_tile = a.o_tma && a.num_splits == 1 && row0 + kM <= w.rows && tok0 >= 0 &&
-                          w.q0 + (row0 + kM - 1) / a.group < a.total_q;
+                          w.q0 + div_group(a, row0 + kM - 1) < a.total_q;
   if (whole_tile) {
     uint8_t* stage = smem + kOffQ + x * kTile + half * kHalf;
 #pragma unroll 1
@@ -636,7 +642,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   const int r = wq * 32 + lane;                // row of tile x = tensor-memory lane
   const int rg = w.mt * 2 * kM + x * kM + r;
   const bool valid = rg < w.rows;
-  const int t = valid ? rg / a.group : 0;
+  const int t = valid ? div_group(a, rg) : 0;
   // keys [k0, lim) are visible to this row
   const int lim = valid ? max(w.k0, min(w.k1, w.L - w.q_len + t + 1)) : w.k0;
   const uint32_t lanes = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -778,7 +784,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       const int nt = w.has_b ? 2 : 1;
       mbar_arrive_expect_tx(&bars->q_full, nt * kTile);
       for (int x = 0; x < nt; ++x) {
-        const int tok = static_cast<int>(w.q0 + (w.mt * 2 * kM + x * kM) / a.group);
+        const int tok = static_cast<int>(w.q0 + div_group(a, w.mt * 2 * kM + x * kM));
         for (int dh = 0; dh < 2; ++dh)
           tma_load_rows(smem + kOffQ + x * kTile + dh * kHalf, &qmap, &bars->q_full, dh * 64,
                         w.g * a.group, tok);
@@ -793,7 +799,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
     const int row = threadIdx.x % (2 * kM), dh = threadIdx.x / (2 * kM);
     const int x = row / kM, r = row % kM;
     const int rg = w.mt * 2 * kM + row;
-    const int t0 = rg / a.group;
+    const int t0 = div_group(a, rg);
     const bool valid = rg < w.rows && w.q0 + t0 >= 0 && w.q0 + t0 < a.total_q;
     const int t = valid ? t0 : 0;
     const int hh = valid ? rg - t * a.group : 0;
@@ -898,6 +904,10 @@ cudaError_t launch_paged_prefill(const CUtensorMap& kmap, const CUtensorMap& vma
   std::memset(&qmap, 0, sizeof(qmap));
   std::memset(&omap, 0, sizeof(omap));
   a.mt_major = a.cu_seqlens_q != nullptr ? 1 : 0;
+  a.group_shift = -1;
+  if (a.group > 0 && (a.group & (a.group - 1)) == 0)
+    for (int s = 0; s < 31; ++s)
+      if ((1 << s) == a.group) a.group_shift = s;
   a.q_tma = encode_rows_map(&qmap, a.q, a.total_q, a.num_q_heads, a.q_stride_h * 2,
                             a.q_stride_t * 2, a.group) ? 1 : 0;
   a.o_tma = (a.num_splits == 1 &&

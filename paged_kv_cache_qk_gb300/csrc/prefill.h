@@ -42,6 +42,7 @@ struct PrefillArgs {
   // sequence, kv head, split) instead of (sequence, split, kv head, row tile
   // descending)
   int32_t mt_major;
+  int32_t group_shift;             // set by launch_paged_prefill: log2(group), or -1
 };
 
 // Shared-memory bytes one CTA of the kernel takes (one CTA per SM).
