@@ -136,6 +136,30 @@ def test_prefill_equals_verify_decode_kernel(lib):
     assert (lse_p - lse_d).abs().max().item() <= 1e-3
 
 
+def test_chained_append_then_prefill(lib):
+    """The benchmarked prefill step: the chunk's q/k normalised and rotated
+    (angles from the per-position table), k/v appended, then the tensor-core
+    prefill over the cache.  The oracle runs the same chain on the same
+    inputs: its norm/RoPE/append, then its paged causal attention."""
+    p = _problem(16, 8, 200, 16, [37, 0, 513], seed=83)
+    q = p.q.clone()
+    kc, vc = p.k_cache.clone(), p.v_cache.clone()
+    q_in, kc_in, vc_in = bits(q), bits(kc), bits(vc)
+    P = int(p.positions.max().item()) + 1
+    table = torch.empty(lib.rope_table_bytes(P), dtype=torch.uint8, device="cuda")
+    lib.rope_table_build(table, P, p.theta)
+    lib.norm_rope_append_cached(q, p.k, p.v, p.positions, p.slot_mapping, p.gamma_q, p.gamma_k,
+                                p.theta, p.eps, kc, vc, table, P)
+    out, lse = _prefill(lib, p, q=q, k_cache=kc, v_cache=vc)
+    qh, kco, vco, _, _ = oracle.norm_rope_append(
+        q_in, bits(p.k), bits(p.v), p.positions.cpu().numpy(), p.slot_mapping.cpu().numpy(),
+        bits(p.gamma_q), bits(p.gamma_k), p.theta, p.eps, kc_in, vc_in, p.block_size)
+    ref, ref_lse = oracle.paged_attention(qh.reshape(p.B, p.q_len, p.Hq, p.D), kco, vco,
+                                          p.block_tables_host, p.seq_lens_host, p.block_size,
+                                          q_len=p.q_len)
+    assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "chained prefill")
+
+
 def test_prefill_without_lse_output(lib):
     """lse_out = NULL: the outputs are the same bits as with it, through both
     output paths (whole row tiles leave by TMA boxes, the ragged last tile by
