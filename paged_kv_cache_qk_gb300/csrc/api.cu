@@ -632,9 +632,11 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
   // few CTAs' work wider (1 x 512: 17.1 -> 15.0 us, 1 x 2048: 19.1 -> 17.1).
   const double target = 0.84 * sm_count * plan.ctas_per_sm;
   const int64_t s_fill = static_cast<int64_t>(target / static_cast<double>(groups * batch) + 0.5);
-  // (a CTA covers one head group: tp * groups pages of work in all)
+  // (a CTA covers one head group: tp * groups pages of work in all; to the
+  // nearest count: the speculative-verify batch of mixed lengths, 32 x
+  // U[2048, 8192] + 5, measured 111 us at 6 splits and 121 us at 7)
   const int64_t s_bal = static_cast<int64_t>(
-      std::ceil(static_cast<double>(p_max) * target / (static_cast<double>(tp) * groups)));
+      std::round(static_cast<double>(p_max) * target / (static_cast<double>(tp) * groups)));
   int64_t S = std::max<int64_t>(1, std::max(s_fill, s_bal));
   const int64_t min_chunk = p_max * block_size <= 2048 ? 64 : 128;
   const int64_t s_min_chunk =
@@ -643,14 +645,16 @@ int32_t pkvqk_choose_num_splits(int32_t batch, int32_t num_kv_heads, int32_t row
   // drop splits that the longest sequence leaves empty
   const int64_t chunk = (p_max + S - 1) / S;
   S = (p_max + chunk - 1) / chunk;
-  // Mixed lengths (the batch holds well under batch x max_seq_len keys) on a
-  // large problem: the balanced schedule (0) measured faster than any split
-  // count (GQA-8 serving batch 91 vs 95 us, verify batch 115 vs 120 us); its
-  // planning prologue (~5 us) does not pay off on small problems.
+  // Strongly mixed lengths (the batch holds well under half of batch x
+  // max_seq_len keys) on a large problem: the balanced schedule (0) measured
+  // faster than any split count (GQA-8 serving batch, fill 0.24: 84 vs 91 us
+  // at its best split); at milder mixes the split count above wins (verify
+  // batch, fill 0.62: 111 us at 6 splits vs 115 balanced).  Its planning
+  // prologue (~5 us) does not pay off on small problems.
   const double fill = static_cast<double>(total_tokens) /
                       (static_cast<double>(batch) * static_cast<double>(max_seq_len));
   const double kv_bytes = static_cast<double>(total_tokens) * num_kv_heads * 512.0;
-  if (fill < 0.85 && kv_bytes >= 128.0 * (1 << 20) && batch * groups >= 8) return 0;
+  if (fill < 0.5 && kv_bytes >= 128.0 * (1 << 20) && batch * groups >= 8) return 0;
   return static_cast<int32_t>(std::max<int64_t>(1, S));
 }
 

@@ -147,9 +147,12 @@ def test_split_heuristic_is_host_only_and_bounded(lib):
     assert lib.choose_num_splits(8, 8, 2, 32768, 8 * 32768, 16, 152) >= 8
     assert lib.choose_num_splits(1, 8, 2, 512, 512, 16, 152) >= 2
     assert lib.choose_num_splits(0, 8, 2, 512, 0, 16, 152) == 1
-    # large batch of mixed lengths: the balanced schedule
+    # large batch of strongly mixed lengths (under half of batch x max keys):
+    # the balanced schedule
     assert lib.choose_num_splits(64, 4, 8, 16384, 230000, 16, 152) == 0
-    assert lib.choose_num_splits(32, 8, 10, 8197, 172000, 16, 152) == 0
+    # a milder mix (the speculative-verify batch, ~0.65 of batch x max keys):
+    # the split count, rounded to the nearest
+    assert lib.choose_num_splits(32, 8, 10, 8197, 172000, 16, 152) == 6
     # small mixed batch: still a split count
     assert lib.choose_num_splits(4, 8, 2, 256, 600, 16, 152) >= 1
 
