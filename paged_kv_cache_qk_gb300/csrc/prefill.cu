@@ -671,28 +671,33 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     float psum = whole ? half_tile<false>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref)
                        : half_tile<true>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref);
     // one reference per row: the higher of the two halves'
-    const float m_row = fmaxf(m_ref, pair_swap(m_ref, slots, xbar, uses, half, r, ok));
+    const float m_other = pair_swap(m_ref, slots, xbar, uses, half, r, ok);
     if (!ok) break;
-    if (__any_sync(0xffffffffu, m_ref < m_row)) {
-      const float f = m_ref < m_row ? pow2_int(m_ref - m_row) : 1.f;
-      scale_p<32>(s_cols, f);
-      psum *= f;
-    }
-    m_ref = m_row;
-    const bool rose = m_row > m_start;         // -inf -> finite counts
-    const float alpha = rose ? pow2_int(m_start - m_row) : 1.f;
-    if (i > 0 && __any_sync(0xffffffffu, rose)) {
-#pragma unroll 1
-      for (int c = 0; c < kHeadDim / 64; ++c) {
-        float o[32];
-        tc5::tmem_ld32(o_cols + c * 32, o);
-        tc5::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-        tc5::tmem_st32(o_cols + c * 32, o);
+    if (__all_sync(0xffffffffu, m_ref == m_start && m_other == m_start)) {
+      l += psum;                               // neither half moved (the usual tile)
+    } else {
+      const float m_row = fmaxf(m_ref, m_other);
+      if (__any_sync(0xffffffffu, m_ref < m_row)) {
+        const float f = m_ref < m_row ? pow2_int(m_ref - m_row) : 1.f;
+        scale_p<32>(s_cols, f);
+        psum *= f;
       }
+      m_ref = m_row;
+      const bool rose = m_row > m_start;       // -inf -> finite counts
+      const float alpha = rose ? pow2_int(m_start - m_row) : 1.f;
+      if (i > 0 && __any_sync(0xffffffffu, rose)) {
+#pragma unroll 1
+        for (int c = 0; c < kHeadDim / 64; ++c) {
+          float o[32];
+          tc5::tmem_ld32(o_cols + c * 32, o);
+          tc5::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc5::tmem_st32(o_cols + c * 32, o);
+        }
+      }
+      l = l * alpha + psum;
     }
-    l = l * alpha + psum;
     // Tail tile: cache slots past the last visible key may hold anything
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
     // their V rows are zeroed (by tile A, each half its dims, before either
