@@ -653,20 +653,30 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
   uint64_t* xbar = &bars->xch[x][wq];
   uint32_t uses = 0;
 
+  // decided once: interior tiles end at or before every row's limit (the
+  // warp's smallest), and only the last tile can reach past key_end (tile A
+  // zeroes the V rows there)
+  int lim_min = lim;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lim_min = min(lim_min, __shfl_xor_sync(0xffffffffu, lim_min, o));
+  const int n = w.ntiles;
+  const int k0 = w.k0;
+  const int tail_tile = (x == 0 && k0 + n * kN > w.key_end) ? n - 1 : -1;
+
   float m_ref = -INFINITY;                     // reference max (log2 units), integer once set
   float l = 0.f;                               // this half's sum of P
   bool ok = true;
-  for (int i = 0; i < w.ntiles; ++i) {
+  for (int i = 0; i < n; ++i) {
     // S_x(i) landed, and with it PV_x(i - 1): O_x is complete up to tile i - 1
     if (!warp_wait(&bars->s_full[x], i & 1)) {
       ok = false;
       break;
     }
     tc5::fence_after_sync();
-    const int kb = w.k0 + i * kN;
+    const int kb = k0 + i * kN;
     const int nvis = min(kN, max(0, lim - kb));   // keys kb .. kb + nvis - 1 visible
     // interior tiles (every row of the warp sees all 128 keys) skip the masks
-    const bool whole = __all_sync(0xffffffffu, nvis == kN);
+    const bool whole = lim_min >= kb + kN;
     const float m_start = m_ref;
     float psum = whole ? half_tile<false>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref)
                        : half_tile<true>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref);
@@ -702,7 +712,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     // (stale or never-written rows); P is 0 there, but 0 x NaN is NaN, so
     // their V rows are zeroed (by tile A, each half its dims, before either
     // PV reads them).
-    if (x == 0 && kb + kN > w.key_end) {
+    if (i == tail_tile) {
       const int s = i & 1;
       if (!warp_wait(&bars->full_v[s], (i >> 1) & 1)) {
         ok = false;
