@@ -186,8 +186,9 @@ PKVQK_API pkvqk_status pkvqk_norm_rope_append_cached(
  * Schedule for pkvqk_paged_decode from host-side facts only (no device
  * read): batch, kv heads, rows per kv head (q_len * Hq/Hkv), the longest
  * sequence, the total key count and the SM count (0 = query the current
- * device).  Returns 0 (the balanced schedule: chosen for large batches of
- * mixed lengths) or a split count in [1, 256]; above 16 rows per kv head
+ * device).  Returns 0 (the balanced schedule: chosen for large batches whose
+ * total keys are under half of batch x longest) or a split count in
+ * [1, 256]; above 16 rows per kv head
  * (run on the tensor-core kernel, see pkvqk_paged_decode) it returns
  * pkvqk_choose_prefill_splits(batch, num_kv_heads, rows_per_kv_head, 1, ...).
  * Source: the "decode routing hint (host side, zero device sync)" of
