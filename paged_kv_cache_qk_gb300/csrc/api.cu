@@ -119,8 +119,9 @@ pkvqk_status get_encoder() {
 //   dims (inner first) = (64 dims, slot, dim half, kv head, block),
 // box = (64, tile_keys slots, halves, heads_per_cta, 1 block), 128-byte
 // swizzle, so the shared-memory tile of one (kv head, half) is tile_keys rows
-// of 128 B.  The decode kernel takes both halves per box, the prefill kernel
-// one (it places the halves of all pages of a key tile in two blocks).
+// of 128 B.  The decode kernel and the prefill kernel's V take both halves
+// per box; the prefill kernel's K takes one (it places the halves of all
+// pages of a key tile in two blocks, as its K-major operand needs).
 pkvqk_status encode_cache_map(CUtensorMap* map, const void* base, const pkvqk_cache_layout& L,
                               int heads_per_cta, int tile_keys, int halves = 2) {
   PKVQK_TRY(get_encoder());
@@ -414,7 +415,7 @@ pkvqk_status run_prefill(const DecodeCall& c, const int32_t* cu_seqlens_q, int64
   const int box_slots = std::min(L.block_size & -L.block_size, 128);
   CUtensorMap kmap, vmap;
   PKVQK_TRY(encode_cache_map(&kmap, c.k_cache, L, 1, box_slots, 1));
-  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, 1, box_slots, 1));
+  PKVQK_TRY(encode_cache_map(&vmap, c.v_cache, L, 1, box_slots, 2));
 
   const int hint = c.max_seq_len_hint > 0 ? c.max_seq_len_hint : static_cast<int>(cap_tokens);
   const int hint_pages = (hint + L.block_size - 1) / L.block_size;

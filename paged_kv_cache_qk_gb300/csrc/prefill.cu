@@ -32,7 +32,7 @@
 //              2^8 (P <= 2^8 otherwise), and writes its 64 output dims;
 //   warp 16    TMA producer: the Q tiles at set-up (one box per row tile and
 //              64-dim half, where q's layout allows), then one box per (page,
-//              64-dim half) of K and of V;
+//              64-dim half) of K and one per page of V;
 //   warp 17    allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
 //              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
@@ -51,7 +51,8 @@
 // the MMA descriptors describe):
 //   Q_A, Q_B  [2 dim halves][128 rows][64 bf16]      2 x 32 KiB
 //   K stage s [2 dim halves][128 keys][64 bf16]      2 x 32 KiB
-//   V stage s  the same                              2 x 32 KiB
+//   V stage s [128 / tb boxes][2 dim halves][tb keys][64 bf16], tb the
+//             slots per box (16 at 16-key pages)     2 x 32 KiB
 //   pair-swap slots [tile][parity][half][128 rows] fp32  4 KiB
 // Tensor memory: S_A at columns 0-127 (P_A over columns 0-31 and 64-95), S_B
 // 128-255 (P_B likewise), O_A 256-383, O_B 384-511.
@@ -128,11 +129,28 @@ __device__ __forceinline__ uint64_t desc_k_major(uint32_t tile, int kk) {
   return tc5::smem_desc_sw128(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
 }
 
-// V tile as the MN-major B operand of O += P V (N = dims, K = keys): 64 dims
-// per swizzled row, the two dim halves kHalf apart (leading offset), 8-key
-// groups 1024 bytes apart (stride offset); 16-key step ks starts 2048 bytes on.
-__device__ __forceinline__ uint64_t desc_v(uint32_t vtile, int ks) {
-  return tc5::smem_desc_sw128(vtile + ks * 2048, kHalf, 1024);
+// Slots per cache box: the largest power of two dividing the page size, at
+// most a key tile; a tile's boxes start at multiples of it, so none crosses a
+// page.  Returns log2.
+__device__ __forceinline__ int box_shift(int block_size) {
+  return __ffs(min(block_size & -block_size, kN)) - 1;
+}
+
+// V stage as the MN-major B operand of O += P V (N = dims, K = keys), one
+// TMA box per tb = 2^tbs keys holding both dim halves: box j at 256 tb j,
+// [2 dim halves][tb keys][64 bf16 swizzled], so the halves are 128 tb bytes
+// apart (leading offset) and 8-key groups 1024 apart (stride offset); the
+// 16-key step ks starts in box 16 ks / tb, 16 ks % tb rows in.  One box per
+// page instead of one per (page, half): at 16-key pages the SM's TMA unit
+// costs ~50 cycles a box on top of ~2.2 a 128-byte row, and V's boxes were
+// half of what held up K.
+__device__ __forceinline__ uint32_t v_step_offset(int ks, int tbs) {
+  const int k = ks * 16;
+  return static_cast<uint32_t>(((k >> tbs) << (tbs + 8)) + ((k & ((1 << tbs) - 1)) << 7));
+}
+__device__ __forceinline__ uint32_t v_row_offset(int key, int half, int tbs) {
+  return static_cast<uint32_t>(((key >> tbs) << (tbs + 8)) + (half << (tbs + 7)) +
+                               ((key & ((1 << tbs) - 1)) << 7));
 }
 
 // 5-D tiled TMA load without an L2 hint: K/V tiles are read by every row tile
@@ -242,28 +260,34 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
                         const CUtensorMap* vmap, uint8_t* smem, Bars* bars, int* issued_out) {
   const int lane = threadIdx.x & 31;
   const int bs = a.block_size;
-  // slots per box: the largest power of two dividing the page size, at most
-  // a key tile; a tile's boxes start at multiples of it, so none crosses a page
-  const int tb = min(bs & -bs, kN);
-  const int ppt = kN / tb;                      // boxes per key tile
+  const int tbs = box_shift(bs);
+  const int tb = 1 << tbs;
+  const int ppt = kN >> tbs;                    // boxes per key tile
   const int32_t* bt = a.block_tables + static_cast<long long>(w.b) * a.max_blocks_per_seq;
   const int oob = static_cast<int>(a.num_blocks);   // past the extent: TMA fills zeros
+  // page id of box `lane` of tile i, when the box holds a visible key; loaded
+  // one tile ahead, so that its latency is not in the chain V(i) -> K(i+1)
+  auto box_visible = [&](int i) { return lane < ppt && w.k0 + i * kN + lane * tb < w.key_end; };
+  auto page_id = [&](int i) {
+    return box_visible(i) ? __ldg(bt + (w.k0 + i * kN + lane * tb) / bs) : oob;
+  };
+  int id_next = w.ntiles > 0 ? page_id(0) : oob;
   int issued = 0;
   for (int i = 0; i < w.ntiles; ++i) {
     const int s = i & 1;
     const uint32_t rel = ((i >> 1) - 1) & 1;         // release of tile i - 2
     uint8_t* kt = smem + kOffK + s * kTile;
     uint8_t* vt = smem + kOffV + s * kTile;
-    int blk = oob, slot0 = 0;
+    int blk = id_next;
+    if (box_visible(i) && (blk < 0 || static_cast<long long>(blk) >= a.num_blocks)) {
+      report(a.status_flags, kFlagBadBlock);
+      blk = oob;
+    }
+    if (i + 1 < w.ntiles) id_next = page_id(i + 1);
+    int slot0 = 0;
     if (lane < ppt) {
       const int key = w.k0 + i * kN + lane * tb;   // first key of box `lane`
-      const int page = key / bs;
-      slot0 = key - page * bs;
-      if (key < w.key_end) {
-        const int id = __ldg(bt + page);
-        if (id >= 0 && static_cast<long long>(id) < a.num_blocks) blk = id;
-        else report(a.status_flags, kFlagBadBlock);
-      }
+      slot0 = key - (key / bs) * bs;
     }
     bool ok = true;
     if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_k[s], rel);
@@ -294,11 +318,8 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
     }
     if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[s], kTile);
     __syncwarp();
-    if (lane < ppt) {
-      tma_load_5d_keep(vt + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 0, w.g, blk);
-      tma_load_5d_keep(vt + kHalf + lane * tb * 128, vmap, &bars->full_v[s], 0, slot0, 1, w.g,
-                       blk);
-    }
+    if (lane < ppt)
+      tma_load_5d_keep(vt + lane * tb * 256, vmap, &bars->full_v[s], 0, slot0, 0, w.g, blk);
     issued = i + 1;
   }
   *issued_out = issued;
@@ -330,7 +351,12 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
   const uint32_t hi = static_cast<uint32_t>(d0 >> 32);
   const uint32_t q_lo = static_cast<uint32_t>(d0);
   const uint32_t k_lo = static_cast<uint32_t>(desc_k_major(smem_addr(smem + kOffK), 0));
-  const uint32_t v_lo = static_cast<uint32_t>(desc_v(smem_addr(smem + kOffV), 0));
+  const int tbs = box_shift(a.block_size);
+  const uint32_t v_lo = static_cast<uint32_t>(
+      tc5::smem_desc_sw128(smem_addr(smem + kOffV), 128u << tbs, 1024));
+  uint32_t v_step[kN / 16];
+#pragma unroll
+  for (int ks = 0; ks < kN / 16; ++ks) v_step[ks] = v_step_offset(ks, tbs) >> 4;
   // S_x(i) = Q_x K_i^T  (the caller has waited for K_i)
   auto mma_s = [&](int x, int i) {
     const int s = i & 1;
@@ -352,8 +378,8 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     // P_x: 16 keys per step = 8 columns of bf16 pairs; keys 64h.. at column 64h
 #pragma unroll
     for (int ks = 0; ks < kN / 16; ++ks)
-      tc5::mma_f16_ts_lh(dst, p0 + (ks >> 2) * (kN / 2) + (ks & 3) * 8, vb + (ks * 2048 >> 4),
-                         hi, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+      tc5::mma_f16_ts_lh(dst, p0 + (ks >> 2) * (kN / 2) + (ks & 3) * 8, vb + v_step[ks], hi,
+                         idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
     if (i == n - 1) tc5::commit(&bars->pv_done[x]);
     if (x == last) tc5::commit(&bars->empty_v[s]);
   };
@@ -719,7 +745,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
         break;
       }
       if (kb + r >= w.key_end) {
-        uint8_t* vrow = smem + kOffV + s * kTile + half * kHalf + r * 128;
+        uint8_t* vrow = smem + kOffV + s * kTile + v_row_offset(r, half, box_shift(a.block_size));
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = z;
