@@ -30,9 +30,11 @@
 //              reference max with the other half once per tile, rescales its
 //              half of O in tensor memory only when the max grew by more than
 //              2^8 (P <= 2^8 otherwise), and writes its 64 output dims;
-//   warp 16    TMA producer: the Q tiles at set-up (one box per row tile and
-//              64-dim half, where q's layout allows), then one box per (page,
-//              64-dim half) of K and one per page of V;
+//   warp 16    TMA producer: Q tile A at set-up (one box per 64-dim half,
+//              where q's layout allows), then one box per (page, 64-dim half)
+//              of K and one per page of V, Q tile B right after K(0) (the SM's
+//              TMA unit takes the boxes one after another, so S_A(0) waits for
+//              two boxes less);
 //   warp 17    allocates the tensor memory; lane 0 issues the MMAs in the
 //              order  S_A(0) S_B(0) | PV_A(i) S_A(i+1) PV_B(i) S_B(i+1) | ...
 //              S_x = Q_x K_i^T  (M 128 rows, N 128 keys, K 128 dims; both
@@ -101,7 +103,7 @@ struct Bars {
   uint64_t pv_done[2];                           // the last O_x += P_x V finished
   uint64_t drain;                                // MMA thread's own completion (timeout path)
   uint64_t xch[2][4];                            // warp pair (tile, lane quadrant) swaps
-  uint64_t q_full;                               // Q tiles landed (TMA)
+  uint64_t q_full[2];                            // Q tile x landed (TMA)
   uint64_t o_staged[2];                          // tile x's output rows staged for TMA
   uint32_t tmem_base;
   int32_t abort;
@@ -257,7 +259,8 @@ __device__ Work decode_work(const PrefillArgs& a) {
 // ------------------------------------------------------------- producer
 
 __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* kmap,
-                        const CUtensorMap* vmap, uint8_t* smem, Bars* bars, int* issued_out) {
+                        const CUtensorMap* vmap, const CUtensorMap* qmap, uint8_t* smem,
+                        Bars* bars, int* issued_out) {
   const int lane = threadIdx.x & 31;
   const int bs = a.block_size;
   const int tbs = box_shift(bs);
@@ -305,6 +308,13 @@ __device__ void produce(const PrefillArgs& a, const Work& w, const CUtensorMap* 
       tma_load_5d_keep(kt + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 0, w.g, blk);
       tma_load_5d_keep(kt + kHalf + lane * tb * 128, kmap, &bars->full_k[s], 0, slot0, 1, w.g,
                        blk);
+    }
+    if (i == 0 && a.q_tma && w.has_b && lane == 0) {
+      mbar_arrive_expect_tx(&bars->q_full[1], kTile);
+      const int tok = static_cast<int>(w.q0 + div_group(a, w.mt * 2 * kM + kM));
+      for (int dh = 0; dh < 2; ++dh)
+        tma_load_rows(smem + kOffQ + kTile + dh * kHalf, qmap, &bars->q_full[1], dh * 64,
+                      w.g * a.group, tok);
     }
     if (lane == 0 && i >= 2) ok = mbar_wait(&bars->empty_v[s], rel);
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -384,13 +394,19 @@ __device__ void issue_mmas(const PrefillArgs& a, const Work& w, uint8_t* smem, B
     if (x == last) tc5::commit(&bars->empty_v[s]);
   };
   bool ok = true;
-  // Q tiles by TMA (issued at set-up)
-  if (a.q_tma && n > 0) ok = mbar_wait(&bars->q_full, 0);
+  // Q tile A by TMA (issued at set-up), tile B after K(0)
+  if (a.q_tma && n > 0) ok = mbar_wait(&bars->q_full[0], 0);
   if (ok && n > 0) ok = mbar_wait(&bars->full_k[0], 0);
   if (ok && n > 0) {
     tc5::fence_after_sync();
     mma_s(0, 0);
-    if (w.has_b) mma_s(1, 0);
+    if (w.has_b) {
+      if (a.q_tma) ok = mbar_wait(&bars->q_full[1], 0);
+      if (ok) {
+        tc5::fence_after_sync();
+        mma_s(1, 0);
+      }
+    }
   }
   for (int i = 0; i < n && ok; ++i) {
     // V_i and K_(i+1) first, while the softmax still works on P_A(i): they
@@ -813,23 +829,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(&bars->pv_done[x], 1);
       mbar_init(&bars->o_staged[x], kSoftmaxWarps / 2);
     }
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full[0], 1);
+    mbar_init(&bars->q_full[1], 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     issued = 0;
     fence_barrier_init();
-    // Q tiles by TMA: one box per (row tile, 64-dim half), rows past q or
+    // Q by TMA: one box per (row tile, 64-dim half), rows past q or
     // before it read as zeros, rows of a following sequence are masked
     if (a.q_tma && w.ntiles > 0) {
       prefetch_tensormap(&qmap);
-      const int nt = w.has_b ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, nt * kTile);
-      for (int x = 0; x < nt; ++x) {
-        const int tok = static_cast<int>(w.q0 + div_group(a, w.mt * 2 * kM + x * kM));
-        for (int dh = 0; dh < 2; ++dh)
-          tma_load_rows(smem + kOffQ + x * kTile + dh * kHalf, &qmap, &bars->q_full, dh * 64,
-                        w.g * a.group, tok);
-      }
+      // tile A now; tile B after K(0), so that S_A(0) waits for two boxes less
+      mbar_arrive_expect_tx(&bars->q_full[0], kTile);
+      const int tok = static_cast<int>(w.q0 + div_group(a, w.mt * 2 * kM));
+      for (int dh = 0; dh < 2; ++dh)
+        tma_load_rows(smem + kOffQ + dh * kHalf, &qmap, &bars->q_full[0], dh * 64,
+                      w.g * a.group, tok);
     }
   }
   if (warp == kMmaWarp) tc5::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -869,12 +884,15 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                    half);
   } else if (warp == kProducerWarp) {
     int n = 0;
-    produce(a, w, &kmap, &vmap, smem, bars, &n);
+    produce(a, w, &kmap, &vmap, &qmap, smem, bars, &n);
     if (threadIdx.x == kProducerWarp * 32) {
       issued = n;
       // the Q copies have landed before the CTA can leave (done long ago
       // unless the MMA thread gave up)
-      if (a.q_tma && w.ntiles > 0) mbar_wait(&bars->q_full, 0);
+      if (a.q_tma && w.ntiles > 0) {
+        mbar_wait(&bars->q_full[0], 0);
+        if (w.has_b) mbar_wait(&bars->q_full[1], 0);
+      }
     }
   } else {
     if ((threadIdx.x & 31) == 0) issue_mmas(a, w, smem, bars, tmem);
