@@ -132,29 +132,29 @@ CPU_BASELINE_WORKLOADS = ("decode_64x8192", "decode_long_8x32768", "decode_gqa8_
 # three warm-up steps), keyed by workload and split count (0: balanced).  A
 # capture describes the kernel sources it was taken with: when the sources
 # hash differently, the bench reports traffic as null.
-SRC = "029c02d74eeaf0b9"
+SRC = "53582c2775d61dfe"
 MEASURED_TRAFFIC = {
-    ("decode_1x2048", 32): {"src": SRC, "bytes": 8468608},
-    ("decode_1x512", 8): {"src": SRC, "bytes": 2176256},
-    ("decode_1x8192", 64): {"src": SRC, "bytes": 33635712},
-    ("decode_32x2048", 4): {"src": SRC, "bytes": 270160256},
-    ("decode_32x512", 4): {"src": SRC, "bytes": 67452288},
-    ("decode_32x8192", 4): {"src": SRC, "bytes": 1075805184},
-    ("decode_64x2048", 2): {"src": SRC, "bytes": 538934272},
-    ("decode_64x512", 2): {"src": SRC, "bytes": 136236288},
-    ("decode_64x8192", 2): {"src": SRC, "bytes": 2149443968},
-    ("decode_8x2048", 16): {"src": SRC, "bytes": 67330816},
-    ("decode_8x512", 8): {"src": SRC, "bytes": 16887936},
-    ("decode_8x8192", 16): {"src": SRC, "bytes": 270072320},
-    ("decode_gqa4_32x8192", 4): {"src": SRC, "bytes": 1075704320},
-    ("decode_gqa8_64", 0): {"src": SRC, "bytes": 468470272},
-    ("decode_gqa8_64x4096", 2): {"src": SRC, "bytes": 539131392},
-    ("decode_long_8x32768", 1): {"src": SRC, "bytes": 1076104576},
-    ("decode_long_8x32768", 8): {"src": SRC, "bytes": 1075547264},
-    ("decode_long_8x32768", 16): {"src": SRC, "bytes": 1075538176},
-    ("decode_long_8x32768", 32): {"src": SRC, "bytes": 1075760896},
-    ("decode_long_8x32768", 128): {"src": SRC, "bytes": 1076087936},
-    ("verify_32x5", 6): {"src": SRC, "bytes": 710270464},
+    ("decode_1x2048", 32): {"src": SRC, "bytes": 8468352},
+    ("decode_1x512", 8): {"src": SRC, "bytes": 2176128},
+    ("decode_1x8192", 64): {"src": SRC, "bytes": 33635584},
+    ("decode_32x2048", 4): {"src": SRC, "bytes": 270230912},
+    ("decode_32x512", 4): {"src": SRC, "bytes": 67453696},
+    ("decode_32x8192", 4): {"src": SRC, "bytes": 1075746432},
+    ("decode_64x2048", 2): {"src": SRC, "bytes": 538666496},
+    ("decode_64x512", 2): {"src": SRC, "bytes": 135940096},
+    ("decode_64x8192", 2): {"src": SRC, "bytes": 2149515264},
+    ("decode_8x2048", 16): {"src": SRC, "bytes": 67362816},
+    ("decode_8x512", 8): {"src": SRC, "bytes": 16885632},
+    ("decode_8x8192", 16): {"src": SRC, "bytes": 270131456},
+    ("decode_gqa4_32x8192", 4): {"src": SRC, "bytes": 1075707776},
+    ("decode_gqa8_64", 0): {"src": SRC, "bytes": 468448000},
+    ("decode_gqa8_64x4096", 2): {"src": SRC, "bytes": 539089920},
+    ("decode_long_8x32768", 1): {"src": SRC, "bytes": 1075767936},
+    ("decode_long_8x32768", 8): {"src": SRC, "bytes": 1075376000},
+    ("decode_long_8x32768", 16): {"src": SRC, "bytes": 1075483776},
+    ("decode_long_8x32768", 32): {"src": SRC, "bytes": 1075882368},
+    ("decode_long_8x32768", 128): {"src": SRC, "bytes": 1076084992},
+    ("verify_32x5", 6): {"src": SRC, "bytes": 710233856},
 }
 
 
