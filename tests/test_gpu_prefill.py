@@ -78,6 +78,12 @@ CASES = [
     # tokens): whole and ragged tiles
     (32, 8, 70, 32, [0, 200]),
     (16, 1, 40, 16, [70, 3]),
+    # pages whose size is not a power of two: V boxes of 32 slots (pages of 96
+    # and 160) and 64 (pages of 192), both dim halves per box, key tiles that
+    # start inside a page
+    (16, 8, 150, 96, [200, 33]),
+    (16, 8, 70, 160, [500, 0]),
+    (16, 8, 130, 192, [90, 401]),
 ]
 
 
