@@ -494,9 +494,15 @@ __device__ __forceinline__ void scale_p(uint32_t taddr, float f) {
 // P pairs to pcol (16 columns per chunk).  kbase = the first key's index in the
 // tile; keys kbase + e >= nvis are masked.  Returns the sum of P (before
 // rounding) against the m_ref in force at the end.
-template <bool kMasked>
+// One pass over this thread's 64 keys of key tile i: two 32-column chunks,
+// each with its max, a rise of the reference when the chunk's max passes it
+// by more than 2^8, the exponentials and the P stores.  The reference is
+// final once the second chunk's max is in: `publish` hands it to the other
+// half of the row there, so that the exchange overlaps that chunk's
+// exponentials instead of following them.
+template <bool kMasked, typename Publish>
 __device__ __forceinline__ float half_tile(uint32_t scol, uint32_t pcol, int kbase, int nvis,
-                                           float sl2, float& m_ref) {
+                                           float sl2, float& m_ref, Publish&& publish) {
   float psum = 0.f;
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -521,6 +527,7 @@ __device__ __forceinline__ float half_tile(uint32_t scol, uint32_t pcol, int kba
       psum *= f;
       m_ref = m_new;
     }
+    if (c == 1) publish(m_ref);
     const float u = (m_ref == -INFINITY) ? 0.f : m_ref;
     const uint64_t scale2 = pack2(sl2, sl2), shift2 = pack2(-u, -u);
     uint64_t acc[4];
@@ -544,20 +551,32 @@ __device__ __forceinline__ float half_tile(uint32_t scol, uint32_t pcol, int kba
   return psum;
 }
 
-// Swap one value per row with the other half of the warp pair: publish v in
-// this half's slot of the current parity, arrive on the pair's barrier, wait
-// (bounded) for the partner's arrival, read its slot.  Slots alternate by
-// parity, so a slot is rewritten only after the partner's next arrival, which
-// follows its read.
-__device__ __forceinline__ float pair_swap(float v, float* slots, uint64_t* bar, uint32_t& uses,
-                                           int half, int r, bool& ok) {
+// Swap one value per row with the other half of the warp pair, in two parts
+// so that work can run in between: publish v in this half's slot of the
+// current parity and arrive on the pair's barrier; then wait (bounded) for
+// the partner's arrival and read its slot.  Slots alternate by parity, so a
+// slot is rewritten only after the partner's next arrival, which follows its
+// read.
+__device__ __forceinline__ void swap_publish(float v, float* slots, uint64_t* bar,
+                                             uint32_t uses, int half, int r) {
   const int p = uses & 1;
   slots[(p * 2 + half) * kM + r] = v;
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ float swap_read(float* slots, uint64_t* bar, uint32_t& uses, int half,
+                                           int r, bool& ok) {
+  const int p = uses & 1;
   ok = warp_wait(bar, p) && ok;
   ++uses;
   return slots[(p * 2 + (half ^ 1)) * kM + r];
+}
+
+__device__ __forceinline__ float pair_swap(float v, float* slots, uint64_t* bar, uint32_t& uses,
+                                           int half, int r, bool& ok) {
+  swap_publish(v, slots, bar, uses, half, r);
+  return swap_read(slots, bar, uses, half, r, ok);
 }
 
 // This thread's half of an output row of tile x: O / l for dims 64h..64h+63
@@ -720,10 +739,11 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     // interior tiles (every row of the warp sees all 128 keys) skip the masks
     const bool whole = lim_min >= kb + kN;
     const float m_start = m_ref;
-    float psum = whole ? half_tile<false>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref)
-                       : half_tile<true>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref);
+    auto publish = [&](float m) { swap_publish(m, slots, xbar, uses, half, r); };
+    float psum = whole ? half_tile<false>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref, publish)
+                       : half_tile<true>(s_cols, s_cols, half * (kN / 2), nvis, sl2, m_ref, publish);
     // one reference per row: the higher of the two halves'
-    const float m_other = pair_swap(m_ref, slots, xbar, uses, half, r, ok);
+    const float m_other = swap_read(slots, xbar, uses, half, r, ok);
     if (!ok) break;
     if (__all_sync(0xffffffffu, m_ref == m_start && m_other == m_start)) {
       l += psum;                               // neither half moved (the usual tile)
