@@ -793,8 +793,7 @@ __device__ void softmax_rows(const PrefillArgs& a, const Work& w, uint8_t* smem,
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->p_full[x]);
   }
-  // write_rows reads the work item from the stack, where the long loop has
-  // let it fall out of L1 (~1 us back from L2): fetch it during the last PV
+  // O_x is complete once the last PV has finished
   if (ok && w.ntiles > 0) {
     ok = warp_wait(&bars->pv_done[x], 0);
     tc5::fence_after_sync();
