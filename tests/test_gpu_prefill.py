@@ -211,10 +211,14 @@ def test_prefill_ignores_non_finite_slots_past_the_end(lib):
     assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "nan tail")
 
 
-def test_prefill_bad_block_id_is_flagged_and_reads_zeros(lib):
-    p = _problem(16, 8, 16, 16, [64], seed=3, extra_blocks=4)
+@pytest.mark.parametrize("prior,page,bad", [(64, 1, "past"), (600, 20, "past"), (600, 20, "neg")],
+                         ids=["tile0", "tile2", "tile2-negative"])
+def test_prefill_bad_block_id_is_flagged_and_reads_zeros(lib, prior, page, bad):
+    # a page of key tile 0 (fetched before the loop) or of key tile 2 (its id
+    # fetched one tile ahead, during tile 1); ids past the extent or negative
+    p = _problem(16, 8, 16, 16, [prior], seed=3, extra_blocks=4)
     bt = p.block_tables.clone()
-    bt[0, 1] = p.num_blocks + 10                       # keys 16..31 -> zeros
+    bt[0, page] = p.num_blocks + 10 if bad == "past" else -5   # 16 keys -> zeros
     flags = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty(p.B, p.q_len, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
     lib.paged_prefill(p.q, p.k_cache, p.v_cache, bt, p.seq_lens, out, q_len=p.q_len,
@@ -224,7 +228,7 @@ def test_prefill_bad_block_id_is_flagged_and_reads_zeros(lib):
     assert torch.isfinite(out.float()).all()
     # the oracle on a cache whose block 1 of the sequence is zero gives the same
     kc, vc = p.k_cache.clone(), p.v_cache.clone()
-    blk = int(p.block_tables_host[0, 1])
+    blk = int(p.block_tables_host[0, page])
     kc[blk] = 0
     vc[blk] = 0
     ref, _ = oracle_attention(p, bits(p.q), k_cache=kc, v_cache=vc)
