@@ -196,16 +196,19 @@ def test_prefill_rows_without_keys(lib):
     assert np.abs(got[~empty] - ref[~empty]).max() <= 2e-2
 
 
-def test_prefill_ignores_non_finite_slots_past_the_end(lib):
+@pytest.mark.parametrize("bs,priors", [(16, [100, 7]), (96, [150, 7]), (192, [300, 41])],
+                         ids=["bs16", "bs96", "bs192"])
+def test_prefill_ignores_non_finite_slots_past_the_end(lib, bs, priors):
     """Cache slots past a sequence's last key (the rest of its last page) may
-    hold anything, NaN included; they must not reach the output."""
-    p = _problem(16, 8, 40, 16, [100, 7], seed=21)
+    hold anything, NaN included; they must not reach the output.  Page sizes
+    16, 96 and 192 put the zeroed V rows in boxes of 16, 32 and 64 slots."""
+    p = _problem(16, 8, 40, bs, priors, seed=21)
     kc, vc = p.k_cache.clone(), p.v_cache.clone()
     for b in range(p.B):
         L = int(p.seq_lens_host[b])
-        last = int(p.block_tables_host[b, (L - 1) // 16])
-        kc[last, L % 16 or 16:] = float("nan")
-        vc[last, L % 16 or 16:] = float("nan")
+        last = int(p.block_tables_host[b, (L - 1) // bs])
+        kc[last, L % bs or bs:] = float("nan")
+        vc[last, L % bs or bs:] = float("nan")
     out, lse = _prefill(lib, p, k_cache=kc, v_cache=vc)
     ref, ref_lse = oracle_attention(p, bits(p.q), k_cache=kc, v_cache=vc)
     assert_attention_close(bits(out), ref, lse.cpu().numpy(), ref_lse, "nan tail")
